@@ -1,0 +1,518 @@
+"""Benchmark of the LayerNorm / RMSNorm backward on GB300.
+
+One step = the whole hot path over one batch of synthetic input: the forward
+(y and the per-row statistics) followed by the backward (the fused per-row dx
++ partial-row kernel, then the fixed-order column reduce of dgamma / dbeta).
+L2 is flushed (a 256 MiB write) before the forward and before the backward of
+every step, outside the timed kernels.
+
+Headline value: achieved HBM GB/s of the backward (minimum bytes: read x, dy,
+gamma and the statistics; write dx, dgamma, dbeta) over its device time,
+measured with CUDA events on the launching stream.  Printed as ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the float64 CPU oracle, timed on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "LN/RMSNorm bwd achieved HBM GB/s (% of GB300 peak) and rows/s at M×N"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: every rank runs the whole workload on its GPU)
+# ---------------------------------------------------------------------------
+def dist_setup(backend: str):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def dist_max(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, traffic record, clocks
+# ---------------------------------------------------------------------------
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("rmsnorm_backward_gb300/csrc/norm_bwd.cu", "rmsnorm_backward_gb300/csrc/gbn_device.cuh",
+                "rmsnorm_backward_gb300/csrc/gbn_launch.h", "rmsnorm_backward_gb300/csrc/gbnorm_api.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the fused backward kernel from an ncu capture,
+    if the capture was taken of the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.gpu = gpu_index
+        self.enabled = enabled
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class Problem:
+    """Device buffers and the three launches of one step for a workload."""
+
+    def __init__(self, w: wl.Workload, device, stream):
+        import rmsnorm_backward_gb300 as gbn
+
+        self.gbn = gbn
+        self.w = w
+        self.dev = device
+        self.stream = stream
+        inp = wl.make_inputs(w)
+        self.host = inp
+        self.x = inp["x"].to(device)
+        self.dy = inp["dy"].to(device)
+        self.gamma = inp["gamma"].to(device)
+        self.beta = inp["beta"].to(device) if w.has_beta else None
+        tdt = wl.TORCH_DTYPES[w.dtype]
+        self.y = torch.empty_like(self.x)
+        self.dx = torch.empty_like(self.x)
+        self.mean = torch.empty(w.M, dtype=torch.float32, device=device) if w.has_beta else None
+        self.rstd = torch.empty(w.M, dtype=torch.float32, device=device)
+        self.dgamma = torch.empty(w.N, dtype=torch.float32, device=device)
+        self.dbeta = torch.empty(w.N, dtype=torch.float32, device=device) if w.has_beta else None
+        self.ws = torch.empty(gbn.bwd_workspace_bytes(w.M, w.N, tdt, w.has_beta, device), dtype=torch.uint8,
+                              device=device)
+        self.tdt = tdt
+
+        # pre-marshalled C-ABI calls for the timed loop (no per-call Python checks)
+        L = gbn.lib()
+        sp = stream.cuda_stream
+        code = gbn.DTYPE_CODES[tdt]
+        M, N, P = w.M, w.N, (lambda t: None if t is None else t.data_ptr())
+        wsb = self.ws.numel()
+        if w.has_beta:
+            self._fwd = (L.ln_fwd, (P(self.x), P(self.gamma), P(self.beta), P(self.y), P(self.mean),
+                                    P(self.rstd), w.eps, M, N, code, sp))
+            self._rows = (L.ln_bwd_rows, (P(self.dy), P(self.x), P(self.gamma), P(self.mean), P(self.rstd),
+                                          P(self.dx), M, N, code, P(self.ws), wsb, sp))
+        else:
+            self._fwd = (L.rms_fwd, (P(self.x), P(self.gamma), P(self.y), P(self.rstd), w.eps, M, N, code, sp))
+            self._rows = (L.rms_bwd_rows, (P(self.dy), P(self.x), P(self.gamma), P(self.rstd), P(self.dx), M, N,
+                                           code, P(self.ws), wsb, sp))
+        self._red = (L.gbn_bwd_reduce, (P(self.ws), wsb, M, N, code, int(w.has_beta), P(self.dgamma),
+                                        P(self.dbeta), sp))
+
+    @staticmethod
+    def _call(fn_args):
+        st = fn_args[0](*fn_args[1])
+        if st != 0:
+            raise RuntimeError(f"{fn_args[0].__name__} returned status {st}")
+
+    def fwd(self):
+        self._call(self._fwd)
+
+    def bwd_rows(self):
+        self._call(self._rows)
+
+    def bwd_reduce(self):
+        self._call(self._red)
+
+    def bwd(self):
+        g = self.gbn
+        if self.w.has_beta:
+            g.ln_bwd(self.dy, self.x, self.gamma, self.mean, self.rstd, dx=self.dx, dgamma=self.dgamma,
+                     dbeta=self.dbeta, workspace=self.ws, stream=self.stream)
+        else:
+            g.rms_bwd(self.dy, self.x, self.gamma, self.rstd, dx=self.dx, dgamma=self.dgamma, workspace=self.ws,
+                      stream=self.stream)
+
+
+def time_steps(prob: Problem, steps: int, warmup: int, flush: torch.Tensor, world: int):
+    """Runs warmup + timed steps; returns per-step event times (ms) of fwd, bwd rows, reduce."""
+    s = prob.stream
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            flush.zero_()
+            prob.fwd()
+            flush.zero_()
+            prob.bwd_rows()
+            prob.bwd_reduce()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for k in range(steps):
+            e = ev[k]
+            flush.zero_()
+            e[0].record(s)
+            prob.fwd()
+            e[1].record(s)
+            flush.zero_()
+            e[2].record(s)
+            prob.bwd_rows()
+            e[3].record(s)
+            prob.bwd_reduce()
+            e[4].record(s)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    fwd = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    rows = np.array([e[2].elapsed_time(e[3]) for e in ev])
+    red = np.array([e[3].elapsed_time(e[4]) for e in ev])
+    return fwd, rows, red, wall
+
+
+def time_e2e(prob: Problem, steps: int):
+    """The backward through the public call with pinned host buffers: H2D of
+    dy, x, gamma and the saved statistics, rms_bwd / ln_bwd, D2H of dx and the
+    parameter gradients, all inside the timed region."""
+    s = prob.stream
+    w = prob.w
+    # statistics saved by a forward, kept on the host like the other inputs
+    with torch.cuda.stream(s):
+        prob.fwd()
+    torch.cuda.synchronize()
+    h_in = {"dy": prob.host["dy"].pin_memory(), "x": prob.host["x"].pin_memory(),
+            "gamma": prob.host["gamma"].pin_memory(), "rstd": prob.rstd.cpu().pin_memory()}
+    if w.has_beta:
+        h_in["mean"] = prob.mean.cpu().pin_memory()
+    h_out = {"dx": torch.empty_like(prob.dx, device="cpu").pin_memory(),
+             "dgamma": torch.empty_like(prob.dgamma, device="cpu").pin_memory()}
+    if w.has_beta:
+        h_out["dbeta"] = torch.empty_like(prob.dbeta, device="cpu").pin_memory()
+    d_in = {"dy": prob.dy, "x": prob.x, "gamma": prob.gamma, "rstd": prob.rstd}
+    if w.has_beta:
+        d_in["mean"] = prob.mean
+    d_out = {"dx": prob.dx, "dgamma": prob.dgamma}
+    if w.has_beta:
+        d_out["dbeta"] = prob.dbeta
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def one():
+        with torch.cuda.stream(s):
+            for k, t in h_in.items():
+                d_in[k].copy_(t, non_blocking=True)
+            prob.bwd()
+            for k, t in h_out.items():
+                t.copy_(d_out[k], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        one()
+    e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w: wl.Workload, target_s: float = 10.0):
+    """The float64 oracle's backward on the host, single thread, on the first
+    rows of the same workload; repeated until ~target_s of CPU work."""
+    import oracle
+
+    rows = min(w.M, max(64, (1 << 22) // w.N))  # a sample of ~4M elements per call
+    sw = w.with_shape(rows, w.N)
+    inp = wl.make_inputs(sw)
+    x = wl.exact_double(inp["x"])
+    dy = wl.exact_double(inp["dy"])
+    g = wl.exact_double(inp["gamma"])
+    if w.has_beta:
+        _, mean, rstd = oracle.ln_fwd(x, g, wl.exact_double(inp["beta"]), w.eps)
+    else:
+        _, rstd = oracle.rms_fwd(x, g, w.eps)
+    calls, t_total = 0, 0.0
+    while t_total < target_s:
+        t0 = time.perf_counter()
+        if w.has_beta:
+            oracle.ln_bwd(dy, x, g, mean, rstd)
+        else:
+            oracle.rms_bwd(dy, x, g, rstd)
+        t_total += time.perf_counter() - t0
+        calls += 1
+    per_call = t_total / calls
+    gbs = wl.bwd_min_bytes(w.op, w.dtype, rows, w.N) / per_call / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "rows_per_s": round(rows / per_call, 1),
+            "sample": (f"float64 oracle backward (C, one thread) on the first {rows} of {w.M} rows "
+                       f"of {w.name}, {calls} calls, {t_total:.1f} s; GB/s counts the {w.dtype} "
+                       "workload's minimum bytes of those rows")}
+
+
+def run_ours(args):
+    rank, world, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.workload]
+    stream = torch.cuda.Stream(device)
+    prob = Problem(w, device, stream)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    import rmsnorm_backward_gb300 as gbn
+
+    G, staged = gbn.bwd_plan(w.M, w.N, prob.tdt, w.has_beta, device)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    with ClockSampler(gpu_index, enabled=not args.no_clocks) as clk:
+        fwd, rows, red, wall = time_steps(prob, args.steps, args.warmup, flush, world)
+    err = gbn.device_error(clear=True, device=device)
+    if err:
+        raise SystemExit(f"kernel error flag set: {err}")
+    bwd = rows + red
+    bwd_s = dist_max(float(bwd.sum()) / 1e3, world, device)
+    rows_s = dist_max(float(rows.sum()) / 1e3, world, device)
+    fwd_s = dist_max(float(fwd.sum()) / 1e3, world, device)
+    K = args.steps
+    bwd_bytes = wl.bwd_min_bytes(w.op, w.dtype, w.M, w.N)
+    fwd_bytes = wl.fwd_min_bytes(w.op, w.dtype, w.M, w.N)
+    value = world * K * bwd_bytes / bwd_s / 1e9
+    peak, peak_src = measured_hbm_peak()
+    # the fused per-row kernel: all algorithmic bytes but the dgamma/dbeta writes
+    rows_bytes = bwd_bytes - 4 * w.N * (2 if w.has_beta else 1)
+    rows_avg = rows_s / K
+    achieved = rows_bytes / rows_avg / 1e9
+    e2e_ms, h2d, d2h = time_e2e(prob, args.e2e_steps)
+    e2e_ms = dist_max(e2e_ms, world, device)
+    out = None
+    if rank == 0:
+        clocks = clk.summary()
+        out = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round((fwd_s + bwd_s) / K * 1e3, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {
+                "workload": w.name, "op": {"ln": "layernorm", "rms": "rmsnorm"}[w.op], "M": w.M, "N": w.N,
+                "eps": w.eps, "inputs": w.describe(), "seed": w.seed,
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "l2": "flushed (256 MiB write) before the forward and before the backward of every step",
+                "G": G, "staged_kernel": staged,
+                "step": "forward (y, stats) then backward (dx + partial rows, then column reduce)",
+                "timed": "value = backward minimum bytes / backward device time (both kernels, CUDA events)",
+            },
+            "rows_per_s": round(world * K * w.M / bwd_s, 1),
+            "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "pct_of_measured_copy": round(100 * value / world / peak, 2),
+            "bwd_us": round(bwd_s / K * 1e6, 3),
+            "bwd_rows_kernel_us": round(rows_avg * 1e6, 3),
+            "reduce_kernel_us": round(dist_max(float(red.sum()) / 1e3, world, device) / K * 1e6, 3)
+            if world == 1 else None,
+            "fwd": {"us": round(fwd_s / K * 1e6, 3), "GB/s": round(K * fwd_bytes / fwd_s / 1e9, 2),
+                    "min_bytes": fwd_bytes},
+            "bwd_min_bytes": bwd_bytes,
+            "roofline": {
+                "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+                "kernel": "bwd_staged_kernel (dx + per-CTA partial rows)",
+                "algorithmic_bytes_per_launch": rows_bytes, "peak_source": peak_src,
+            },
+            "e2e": {"value": round(world * bwd_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4),
+                    "what": "pinned host -> device inputs, rms_bwd/ln_bwd, device -> pinned host outputs"},
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+            "wall_s_timed_region": round(wall, 3),
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The float64 CPU oracle as the reference arm (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    w = wl.WORKLOADS[args.workload]
+    rows = min(w.M, max(16, (1 << 20) // w.N))  # ~1M elements per step
+    sw = w.with_shape(rows, w.N)
+    inp = wl.make_inputs(sw)
+    x, dy, g = (wl.exact_double(inp[k]) for k in ("x", "dy", "gamma"))
+    if w.has_beta:
+        _, mean, rstd = oracle.ln_fwd(x, g, wl.exact_double(inp["beta"]), w.eps)
+    else:
+        _, rstd = oracle.rms_fwd(x, g, w.eps)
+
+    def step():
+        if w.has_beta:
+            oracle.ln_bwd(dy, x, g, mean, rstd)
+        else:
+            oracle.rms_bwd(dy, x, g, rstd)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps * wl.bwd_min_bytes(w.op, w.dtype, rows, w.N) / dt / 1e9
+    sample = (f"float64 oracle backward (C, one thread) on the first {rows} of {w.M} rows of {w.name} per step; "
+              f"GB/s counts the {w.dtype} workload's minimum bytes of those rows")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "sample_rows": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * gbnorm.h -- C ABI of the GB300 (sm_103a) LayerNorm / RMSNorm forward and
+ * backward library (libgbnorm.so).
+ *
+ * The operations are the ones defined on the page "Norm backward in Triton --
+ * the dγ/dβ reduction", section "The gradients" (and, with the same formulas,
+ * "Norm & activation backward", section "LayerNorm backward, derived"):
+ *
+ *   LayerNorm, per row x of length N:
+ *     mean = sum(x)/N,  var = sum((x-mean)^2)/N  (biased, after the mean),
+ *     rstd = 1/sqrt(var + eps),  xhat = (x-mean)*rstd,  y = gamma*xhat + beta
+ *   RMSNorm, per row:
+ *     rstd = 1/sqrt(sum(x^2)/N + eps),  xhat = x*rstd,  y = gamma*xhat
+ *   Backward, with dyhat = dy*gamma:
+ *     dx = rstd*(dyhat - mean(dyhat) - xhat*mean(dyhat*xhat))
+ *          (RMSNorm: without the mean(dyhat) term)
+ *     dgamma[j] = sum over rows of dy*xhat,  dbeta[j] = sum over rows of dy
+ *
+ * The backward recomputes xhat from the saved per-row mean / rstd instead of
+ * reading a stored xhat ("Norm & activation backward", section "Half one").
+ * dgamma / dbeta are reduced deterministically: each CTA owns a contiguous
+ * block of rows and writes one fp32 partial row into a caller-provided
+ * [G, N] workspace; a second kernel sums the G partial rows per column in a
+ * fixed order ("Norm backward in Triton", section "The hard half", the
+ * disjoint-row-block variant).  No floating-point atomics are used, so
+ * dgamma / dbeta are bit-identical from run to run for the same inputs,
+ * shapes, dtype, device and buffer alignment.
+ *
+ * Conventions shared by every call:
+ *   - Tensors are row-major and contiguous: element (r, j) of an [M, N] tensor
+ *     is at index r*N + j.  gamma, beta, dgamma, dbeta are length N; mean and
+ *     rstd are length M.
+ *   - x, y, dy, dx, gamma, beta are of type `dtype` (gbn_dtype).  mean, rstd,
+ *     dgamma, dbeta are always float32.
+ *   - Every pointer is DEVICE memory owned by the caller, on the current CUDA
+ *     device.  The library allocates nothing, frees nothing and never
+ *     synchronises: each call only enqueues kernels on `stream` (0 = the
+ *     legacy default stream) and returns.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - Arithmetic is float32 with float32 reductions; results stored in
+ *     fp16 / bf16 are rounded to nearest even.
+ *   - 16-byte aligned pointers with N*sizeof(dtype) a multiple of 16 take the
+ *     bulk-copy (TMA) staged kernels; anything else takes a plain-load kernel
+ *     with the same results up to float32 rounding order.
+ *   - Return value: GBN_OK (0) or a gbn_status code.  Argument errors are
+ *     detected on the host before anything is enqueued.  GBN_ECUDA means a
+ *     launch or a CUDA query failed (the CUDA error is cleared).  Faults of
+ *     kernels already enqueued surface at the caller's next synchronisation,
+ *     as with any CUDA call.
+ */
+#ifndef GBNORM_H
+#define GBNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GBN_F32 = 0,  /* float32 storage                     */
+    GBN_F16 = 1,  /* IEEE binary16 storage               */
+    GBN_BF16 = 2  /* bfloat16 storage                    */
+} gbn_dtype;
+
+typedef enum {
+    GBN_OK = 0,
+    GBN_EINVAL = 1,     /* null pointer, M < 0, N < 1 or too large, bad eps   */
+    GBN_EDTYPE = 2,     /* dtype not one of gbn_dtype                         */
+    GBN_EWORKSPACE = 4, /* workspace_bytes below gbn_bwd_workspace_bytes()    */
+    GBN_ECUDA = 5,      /* a CUDA launch or query failed                      */
+    GBN_EDEVICE = 6     /* a kernel gave up on a bounded wait (see below)     */
+} gbn_status;
+
+/* Largest N accepted by every call. */
+#define GBN_MAX_N (1 << 24)
+
+/*
+ * Bytes of device workspace the backward (ln_bwd / rms_bwd and their two
+ * phases) needs for an [M, N] problem of `dtype` on the CURRENT device;
+ * has_beta = 1 for LayerNorm (dgamma and dbeta partials), 0 for RMSNorm.
+ * The size depends on the device's SM count.  The workspace may have any
+ * alignment.  Returns 0 if M <= 0 (no workspace is needed) or the arguments
+ * are invalid.
+ */
+size_t gbn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta);
+
+/*
+ * LayerNorm forward ("Norm backward in Triton", "The gradients", forward
+ * line; "05: Layer norm", kernel ln_fwd: mean first, then the biased
+ * variance of the centred row, eps under the root).
+ *   x [M,N] dtype (in), gamma [N], beta [N] dtype (in),
+ *   y [M,N] dtype (out), mean [M] f32 (out), rstd [M] f32 (out).
+ *   eps >= 0 and finite.  M = 0 is a no-op.
+ */
+int ln_fwd(const void *x, const void *gamma, const void *beta, void *y,
+           float *mean, float *rstd, float eps, int64_t M, int64_t N,
+           int dtype, cudaStream_t stream);
+
+/*
+ * RMSNorm forward ("Norm backward in Triton", "The gradients", RMSNorm
+ * paragraph): rstd = 1/sqrt(mean(x^2) + eps), y = gamma * x * rstd.
+ *   x [M,N] (in), gamma [N] (in), y [M,N] (out), rstd [M] f32 (out).
+ */
+int rms_fwd(const void *x, const void *gamma, void *y, float *rstd, float eps,
+            int64_t M, int64_t N, int dtype, cudaStream_t stream);
+
+/*
+ * LayerNorm backward ("Norm backward in Triton", "The gradients": dx, dgamma,
+ * dbeta lines; the dx kernel recomputes xhat from the saved statistics).
+ *   dy, x [M,N] dtype (in); gamma [N] dtype (in); mean, rstd [M] f32 (in,
+ *   as written by ln_fwd); dx [M,N] dtype (out); dgamma, dbeta [N] f32 (out).
+ *   eps is not used (rstd already holds it); it is accepted so that the four
+ *   calls share one parameter list.
+ *   workspace: device scratch of at least gbn_bwd_workspace_bytes(M, N,
+ *   dtype, 1) bytes, owned by the caller; its contents on entry do not
+ *   matter and on return are the per-CTA partials.  It must not be used by
+ *   another call that runs concurrently.
+ *   M = 0: dgamma and dbeta are set to zero, nothing else is touched.
+ */
+int ln_bwd(const void *dy, const void *x, const void *gamma, const float *mean,
+           const float *rstd, void *dx, float *dgamma, float *dbeta, float eps,
+           int64_t M, int64_t N, int dtype, void *workspace,
+           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * RMSNorm backward: LayerNorm's without the mean and without the mean(dyhat)
+ * term, and without dbeta.  Arguments as for ln_bwd; the workspace size is
+ * gbn_bwd_workspace_bytes(M, N, dtype, 0).
+ */
+int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
+            void *dx, float *dgamma, float eps, int64_t M, int64_t N, int dtype,
+            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The two phases of the backward, for callers that time or overlap them
+ * separately.  *_bwd_rows runs only the fused per-row kernel: dx, plus the
+ * per-CTA partial rows written into `workspace` ("Norm backward in Triton",
+ * "The hard half": one partial row per block of rows).  gbn_bwd_reduce then
+ * sums those partial rows per column in a fixed order into dgamma (and
+ * dbeta when has_beta = 1).  Running ln_bwd_rows then gbn_bwd_reduce on one
+ * stream, with the same (M, N, dtype) and workspace, is exactly ln_bwd.
+ */
+int ln_bwd_rows(const void *dy, const void *x, const void *gamma,
+                const float *mean, const float *rstd, void *dx, int64_t M,
+                int64_t N, int dtype, void *workspace, size_t workspace_bytes,
+                cudaStream_t stream);
+int rms_bwd_rows(const void *dy, const void *x, const void *gamma,
+                 const float *rstd, void *dx, int64_t M, int64_t N, int dtype,
+                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+int gbn_bwd_reduce(const void *workspace, size_t workspace_bytes, int64_t M,
+                   int64_t N, int dtype, int has_beta, float *dgamma,
+                   float *dbeta, cudaStream_t stream);
+
+/*
+ * Describes the launch the backward takes for an [M, N] problem on the
+ * current device: *G = number of row blocks (CTAs, rows of the partial
+ * workspace), *staged = 1 if 16-byte aligned buffers take the bulk-copy
+ * staged kernel (0 = plain-load kernel for every alignment).  Either output
+ * pointer may be NULL.  Returns a gbn_status.
+ */
+int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G,
+                 int *staged);
+
+/*
+ * Every wait inside the library's kernels (on a shared-memory barrier that
+ * a bulk copy completes) gives up after about two seconds; the kernel then
+ * records an error code in a per-device flag, drains its own copies with
+ * another bounded wait and returns instead of hanging.  This call
+ * synchronises the current device, returns the flag (0 = no error) and, if
+ * clear != 0, resets it.  GBN_ECUDA (as a negative number) if the
+ * synchronisation or the read fails.
+ */
+int gbn_device_error(int clear);
+
+/* A static, human-readable name of a gbn_status code. */
+const char *gbn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBNORM_H */

@@ -1,0 +1,272 @@
+"""LayerNorm / RMSNorm forward and backward on GB300 (sm_103a).
+
+Thin Python binding of the C-ABI library ``libgbnorm.so`` (declared in
+``include/gbnorm.h``).  Every step of the computation runs in the library's
+CUDA kernels; this module only checks tensor metadata, allocates outputs with
+PyTorch when the caller gives none, and passes raw device pointers, sizes and
+the current CUDA stream through ctypes.  There is no CPU or PyTorch fallback:
+if the library is not built, or a tensor is not on a CUDA device, the call
+raises.
+
+Names follow the pages' notation: ``ln_fwd``, ``rms_fwd`` produce ``y`` and
+the per-row statistics (``mean``, ``rstd``); ``ln_bwd``, ``rms_bwd`` take
+``dy`` and the saved statistics and produce ``dx``, ``dgamma`` (and
+``dbeta``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "GbnError", "lib", "library_path", "ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd",
+    "ln_bwd_rows", "rms_bwd_rows", "bwd_reduce", "bwd_workspace_bytes", "bwd_plan",
+    "device_error", "status_string", "DTYPE_CODES",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "_lib", "libgbnorm.so")
+
+DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+GBN_OK = 0
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+
+class GbnError(RuntimeError):
+    """A libgbnorm call returned a non-zero gbn_status."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    L.gbn_bwd_workspace_bytes.argtypes = [_i64, _i64, _int, _int]
+    L.gbn_bwd_workspace_bytes.restype = _sz
+    L.ln_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp]
+    L.rms_fwd.argtypes = [_vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp]
+    L.ln_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, _vp]
+    L.rms_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, _vp]
+    L.ln_bwd_rows.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
+    L.rms_bwd_rows.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
+    L.gbn_bwd_reduce.argtypes = [_vp, _sz, _i64, _i64, _int, _int, _vp, _vp, _vp]
+    L.gbn_bwd_plan.argtypes = [_i64, _i64, _int, _int, ctypes.POINTER(_int), ctypes.POINTER(_int)]
+    L.gbn_device_error.argtypes = [_int]
+    L.gbn_status_string.argtypes = [_int]
+    L.gbn_status_string.restype = ctypes.c_char_p
+    for name in ("ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd", "ln_bwd_rows", "rms_bwd_rows",
+                 "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error"):
+        getattr(L, name).restype = _int
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgbnorm.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(library_path):
+                    raise RuntimeError(
+                        f"libgbnorm.so is not built ({library_path}); run "
+                        "`python -m rmsnorm_backward_gb300.build` or __graft_entry__.build()")
+                _lib = _declare(ctypes.CDLL(library_path))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gbn_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != GBN_OK:
+        raise GbnError(fn, status)
+
+
+def _rows(t: torch.Tensor, name: str) -> Tuple[int, int]:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dim() < 1:
+        raise ValueError(f"{name} must have a feature dimension")
+    N = t.shape[-1]
+    return (t.numel() // N if N else 0), N
+
+
+def _code(t: torch.Tensor) -> int:
+    try:
+        return DTYPE_CODES[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def _vec(t: Optional[torch.Tensor], name: str, n: int, dtype: torch.dtype, device) -> None:
+    if t is None:
+        return
+    if t.dtype != dtype or t.numel() != n or not t.is_contiguous() or t.device != device:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of {n} elements on {device}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def bwd_workspace_bytes(M: int, N: int, dtype: torch.dtype, has_beta: bool, device=None) -> int:
+    """Workspace bytes the backward needs on ``device`` (default: current)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(lib().gbn_bwd_workspace_bytes(M, N, DTYPE_CODES[dtype], int(has_beta)))
+
+
+def bwd_plan(M: int, N: int, dtype: torch.dtype, has_beta: bool, device=None) -> Tuple[int, bool]:
+    """(G, staged): the number of row blocks and whether aligned buffers take the staged kernel."""
+    G, staged = _int(0), _int(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check("gbn_bwd_plan", lib().gbn_bwd_plan(M, N, DTYPE_CODES[dtype], int(has_beta),
+                                                  ctypes.byref(G), ctypes.byref(staged)))
+    return G.value, bool(staged.value)
+
+
+def device_error(clear: bool = True, device=None) -> int:
+    """Synchronises the device and returns (and by default clears) the kernels' error flag."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(lib().gbn_device_error(int(clear)))
+
+
+def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float, *,
+           y: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
+           rstd: Optional[torch.Tensor] = None, stream=None):
+    """LayerNorm forward over the last dimension. Returns (y, mean, rstd)."""
+    M, N = _rows(x, "x")
+    y = torch.empty_like(x) if y is None else y
+    mean = torch.empty(M, dtype=torch.float32, device=x.device) if mean is None else mean
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device) if rstd is None else rstd
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        _vec(t, name, N, x.dtype, x.device)
+    _vec(mean, "mean", M, torch.float32, x.device)
+    _vec(rstd, "rstd", M, torch.float32, x.device)
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous():
+        raise ValueError("y must be contiguous, with x's shape and dtype")
+    with torch.cuda.device(x.device):
+        _check("ln_fwd", lib().ln_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
+                                      float(eps), M, N, _code(x), _stream(x.device, stream)))
+    return y, mean, rstd
+
+
+def rms_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, *, y: Optional[torch.Tensor] = None,
+            rstd: Optional[torch.Tensor] = None, stream=None):
+    """RMSNorm forward over the last dimension. Returns (y, rstd)."""
+    M, N = _rows(x, "x")
+    y = torch.empty_like(x) if y is None else y
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device) if rstd is None else rstd
+    _vec(gamma, "gamma", N, x.dtype, x.device)
+    _vec(rstd, "rstd", M, torch.float32, x.device)
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous():
+        raise ValueError("y must be contiguous, with x's shape and dtype")
+    with torch.cuda.device(x.device):
+        _check("rms_fwd", lib().rms_fwd(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), float(eps), M, N,
+                                        _code(x), _stream(x.device, stream)))
+    return y, rstd
+
+
+def _bwd_args(dy, x, gamma, stats, dx, ln):
+    M, N = _rows(x, "x")
+    if dy.shape != x.shape or dy.dtype != x.dtype or not dy.is_contiguous() or dy.device != x.device:
+        raise ValueError("dy must be contiguous, with x's shape, dtype and device")
+    _vec(gamma, "gamma", N, x.dtype, x.device)
+    for name, t in stats:
+        _vec(t, name, M, torch.float32, x.device)
+    dx = torch.empty_like(x) if dx is None else dx
+    if dx.shape != x.shape or dx.dtype != x.dtype or not dx.is_contiguous():
+        raise ValueError("dx must be contiguous, with x's shape and dtype")
+    return M, N, dx
+
+
+def _workspace(workspace, M, N, x, ln):
+    need = bwd_workspace_bytes(M, N, x.dtype, ln, x.device)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    if workspace.device != x.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on x's device")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor, *,
+           dx=None, dgamma=None, dbeta=None, workspace=None, stream=None):
+    """LayerNorm backward from the saved mean / rstd. Returns (dx, dgamma, dbeta); grads are fp32."""
+    M, N, dx = _bwd_args(dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx, True)
+    dgamma = torch.empty(N, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
+    dbeta = torch.empty(N, dtype=torch.float32, device=x.device) if dbeta is None else dbeta
+    _vec(dgamma, "dgamma", N, torch.float32, x.device)
+    _vec(dbeta, "dbeta", N, torch.float32, x.device)
+    workspace, wsb = _workspace(workspace, M, N, x, True)
+    with torch.cuda.device(x.device):
+        _check("ln_bwd", lib().ln_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                      _ptr(dgamma), _ptr(dbeta), 0.0, M, N, _code(x), _ptr(workspace), wsb,
+                                      _stream(x.device, stream)))
+    return dx, dgamma, dbeta
+
+
+def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: torch.Tensor, *,
+            dx=None, dgamma=None, workspace=None, stream=None):
+    """RMSNorm backward from the saved rstd. Returns (dx, dgamma); dgamma is fp32."""
+    M, N, dx = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx, False)
+    dgamma = torch.empty(N, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
+    _vec(dgamma, "dgamma", N, torch.float32, x.device)
+    workspace, wsb = _workspace(workspace, M, N, x, False)
+    with torch.cuda.device(x.device):
+        _check("rms_bwd", lib().rms_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
+                                        0.0, M, N, _code(x), _ptr(workspace), wsb, _stream(x.device, stream)))
+    return dx, dgamma
+
+
+def ln_bwd_rows(dy, x, gamma, mean, rstd, *, dx=None, workspace, stream=None):
+    """Phase 1 of ln_bwd: dx and the per-CTA partial rows in ``workspace``. Returns dx."""
+    M, N, dx = _bwd_args(dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx, True)
+    workspace, wsb = _workspace(workspace, M, N, x, True)
+    with torch.cuda.device(x.device):
+        _check("ln_bwd_rows", lib().ln_bwd_rows(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd),
+                                                _ptr(dx), M, N, _code(x), _ptr(workspace), wsb,
+                                                _stream(x.device, stream)))
+    return dx
+
+
+def rms_bwd_rows(dy, x, gamma, rstd, *, dx=None, workspace, stream=None):
+    """Phase 1 of rms_bwd: dx and the per-CTA partial rows in ``workspace``. Returns dx."""
+    M, N, dx = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx, False)
+    workspace, wsb = _workspace(workspace, M, N, x, False)
+    with torch.cuda.device(x.device):
+        _check("rms_bwd_rows", lib().rms_bwd_rows(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), M, N,
+                                                  _code(x), _ptr(workspace), wsb, _stream(x.device, stream)))
+    return dx
+
+
+def bwd_reduce(workspace: torch.Tensor, M: int, N: int, dtype: torch.dtype, has_beta: bool, *,
+               dgamma: torch.Tensor, dbeta: Optional[torch.Tensor] = None, stream=None):
+    """Phase 2 of the backward: the fixed-order column sum of the partial rows."""
+    dev = workspace.device
+    _vec(dgamma, "dgamma", N, torch.float32, dev)
+    if has_beta:
+        _vec(dbeta, "dbeta", N, torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check("gbn_bwd_reduce", lib().gbn_bwd_reduce(
+            _ptr(workspace), workspace.numel() * workspace.element_size(), M, N, DTYPE_CODES[dtype],
+            int(has_beta), _ptr(dgamma), _ptr(dbeta) if has_beta else None, _stream(dev, stream)))

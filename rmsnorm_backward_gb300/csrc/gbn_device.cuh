@@ -1,0 +1,269 @@
+// gbn_device.cuh -- device-side building blocks shared by the forward and
+// backward kernels: 16-byte vector load/store traits for the three storage
+// dtypes, inline-PTX wrappers for shared-memory mbarriers and 1-D bulk
+// (TMA) copies, named barriers, and bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbn {
+
+// ---------------------------------------------------------------------------
+// storage dtypes: a 16-byte vector holds kVec elements
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Traits;
+
+template <>
+struct Traits<float> {
+    static constexpr int kVec = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+    __device__ __forceinline__ static float load1(const float *p) { return *p; }
+    __device__ __forceinline__ static void store1(float *p, float v) { *p = v; }
+};
+
+template <>
+struct Traits<__half> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 p = __half22float2(h);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ __forceinline__ static float load1(const __half *p) { return __half2float(*p); }
+    __device__ __forceinline__ static void store1(__half *p, float v) { *p = __float2half_rn(v); }
+};
+
+template <>
+struct Traits<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // a bf16 is the upper half of the float with the same bits
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    __device__ __forceinline__ static void store1(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+// ---------------------------------------------------------------------------
+// error flag: one per device, read and cleared by gbn_device_error()
+// ---------------------------------------------------------------------------
+enum : int {
+    kErrWaitFull = 1,   // a bulk copy did not complete within the wait limit
+    kErrDrain = 2,      // copies still in flight at exit after the wait limit
+};
+
+// the flag lives in norm_bwd.cu; kernels receive its address in their
+// parameter block (no relocatable device code needed)
+__device__ __forceinline__ void record_error(int *flag, int code) { atomicCAS(flag, 0, code); }
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// makes barrier initialisation visible to the async (bulk copy) proxy
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same memory
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of `bar` with the given parity to complete, giving up
+// after ~limit_ns (checked on the global timer) or 2^28 polls, whichever
+// comes first.  Returns false on giving up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < (1u << 28); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes` of
+// transaction count on `bar`.  dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read exactly once (evict first)
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// barrier over `count` threads (a multiple of 32) of this CTA, id in 1..15
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+// 16-byte global load through the read-only path, no L1 allocation
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16-byte streaming global store
+__device__ __forceinline__ void st_global_cs_v4(void *p, const uint4 &v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+// butterfly sum over the 32 lanes; every lane ends with the same bits (each
+// step adds the same two operands on both partner lanes)
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Row partition of M rows over G blocks: block b owns [row_begin, row_begin + rows).
+__host__ __device__ __forceinline__ void block_rows(int64_t M, int G, int b, int64_t &row_begin, int &rows) {
+    const int64_t base = M / G;
+    const int64_t rem = M % G;
+    row_begin = b * base + (b < rem ? b : rem);
+    rows = static_cast<int>(base + (b < rem ? 1 : 0));
+}
+
+}  // namespace gbn
+
+namespace gbn {
+
+// Sums the NQ values of every thread of one row slot (W warps, tpr = 32*W
+// threads, named barrier bar_id) and leaves the totals in v on every thread
+// of the slot, summed warp by warp in a fixed order.  `buf` is this slot's
+// scratch of W*NQ floats; consecutive calls must alternate buffers.  Also
+// returns, uniformly over the slot, whether any of its threads passed
+// give_up = true (a wait that ran out); `flag` is the slot's abort flag.
+template <int NQ>
+__device__ __forceinline__ bool slot_reduce(float (&v)[NQ], float *buf, volatile int *flag, bool give_up,
+                                            int W, int warp, int lane, int bar_id, int tpr) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) v[q] = warp_sum(v[q]);
+    if (W == 1) return __any_sync(0xffffffffu, give_up) != 0;
+    if (give_up) *flag = 1;
+    if (lane == 0) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) buf[warp * NQ + q] = v[q];
+    }
+    named_barrier(bar_id, tpr);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        float s = buf[q];
+        for (int w = 1; w < W; ++w) s += buf[w * NQ + q];
+        v[q] = s;
+    }
+    return *flag != 0;
+}
+
+// Block-wide sum for the plain-load kernels (blockDim.x = 32 * warps); every
+// thread gets the same bits.  `sm` holds one float per warp.
+__device__ __forceinline__ float block_sum(float v, float *sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    if (lane == 0) sm[warp] = v;
+    __syncthreads();
+    float s = sm[0];
+    for (int w = 1; w < nw; ++w) s += sm[w];
+    __syncthreads();
+    return s;
+}
+
+}  // namespace gbn

@@ -1,0 +1,99 @@
+// gbn_launch.h -- kernel parameter blocks and the launch functions that the
+// C ABI layer (gbnorm_api.cu) calls.  Internal to libgbnorm.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gbn {
+
+// threads of the bulk-copy (TMA) staged kernels and of the plain-load ones
+constexpr int kRingThreads = 512;
+constexpr int kGenericThreads = 256;
+// most rows one CTA takes; its rows' statistics are staged in shared memory
+constexpr int kMaxRowsPerCta = 2048;
+// most 16-byte vectors one thread holds per row in the staged kernels
+constexpr int kMaxVecPerThread = 4;
+
+struct FwdParams {
+    const void *x;
+    const void *gamma;
+    const void *beta;  // LayerNorm only
+    void *y;
+    float *mean;       // LayerNorm only
+    float *rstd;
+    float eps;
+    int64_t M;
+    int N;
+    int G;          // CTAs; CTA b takes the rows of block_rows(M, G, b)
+    int tpr;        // staged: threads per row slot (multiple of 32)
+    int stages;     // staged: ring stages per row slot
+    int stat_rows;  // unused by the forward (kept for a uniform layout)
+    int *err;       // the device's error flag
+};
+
+struct BwdParams {
+    const void *dy;
+    const void *x;
+    const void *gamma;
+    const float *mean;  // LayerNorm only
+    const float *rstd;
+    void *dx;
+    float *part;        // [G][ldp] dgamma partials, then [G][ldp] dbeta partials (LayerNorm)
+    int64_t M;
+    int N;
+    int ldp;            // row stride of the partials, in floats (multiple of 4)
+    int G;
+    int tpr;
+    int stages;
+    int stat_rows;      // capacity, in rows, of the staged statistics
+    int *err;           // the device's error flag
+};
+
+// Shared-memory layout of the staged kernels, computed identically on the
+// host (to size the launch) and on the device (to carve the buffer).
+struct RingLayout {
+    size_t ring_off, ring_bytes;  // [slots][stages][stage_bytes]; reused for the partial combine
+    size_t bar_off;               // [slots][stages] mbarriers
+    size_t stat_off;              // [stat_rows] rstd, then [stat_rows] mean (LayerNorm)
+    size_t red_off;               // [slots][4][warps per slot][2] floats
+    size_t flag_off;              // [slots] ints: per-slot abort flags
+    size_t total;
+};
+
+__host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline RingLayout ring_layout(bool bwd, bool ln, int es, int N, int tpr, int stages,
+                                                  int stat_rows, int threads) {
+    RingLayout L;
+    const int slots = threads / tpr;
+    const size_t stage_bytes = (bwd ? 2u : 1u) * (size_t)N * es;
+    size_t ring = (size_t)slots * stages * stage_bytes;
+    if (bwd) {
+        const size_t combine = (size_t)slots * round_up((size_t)N, 4) * 4 * (ln ? 2 : 1);
+        if (slots > 1 && combine > ring) ring = combine;
+    }
+    L.ring_off = 0;
+    L.ring_bytes = round_up(ring, 128);
+    L.bar_off = L.ring_bytes;
+    L.stat_off = L.bar_off + round_up((size_t)slots * stages * 8, 16);
+    L.red_off = L.stat_off + round_up((size_t)stat_rows * 4 * (ln ? 2 : 1), 16);
+    L.flag_off = L.red_off + (size_t)slots * 4 * (tpr / 32) * 2 * 4;
+    L.total = round_up(L.flag_off + (size_t)slots * 4, 128);
+    return L;
+}
+
+// dtype codes as in gbnorm.h
+cudaError_t launch_fwd_staged(int dtype, bool ln, int nv, const FwdParams &p, size_t smem, cudaStream_t s);
+cudaError_t launch_fwd_plain(int dtype, bool ln, const FwdParams &p, cudaStream_t s);
+cudaError_t launch_bwd_staged(int dtype, bool ln, int nv, const BwdParams &p, size_t smem, cudaStream_t s);
+cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_t s);
+cudaError_t launch_colsum(const float *part, int G, int ldp, int N, float *dgamma, float *dbeta,
+                          cudaStream_t s);
+
+// the current device's error flag: its device address, and a synchronising read
+cudaError_t error_flag_address(int **addr);
+cudaError_t read_error_flag(int *value, bool clear);
+
+}  // namespace gbn

@@ -1,0 +1,302 @@
+// gbnorm_api.cu -- the extern "C" entry points of libgbnorm.so declared in
+// include/gbnorm.h: argument checks, choice of kernel and launch shape, and
+// the workspace contract of the deterministic dgamma / dbeta reduction.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cstdlib>
+
+#include "gbn_launch.h"
+#include "gbnorm.h"
+
+namespace gbn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+    int sms = 0;
+    int smem_optin = 0;
+    int *err = nullptr;
+};
+
+// per-device properties, filled once per device (racing fills write the same values)
+DevInfo g_dev[kMaxDevices];
+std::atomic<int> g_dev_ready[kMaxDevices];
+
+int device_info(DevInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GBN_ECUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GBN_ECUDA;
+    if (!g_dev_ready[dev].load(std::memory_order_acquire)) {
+        DevInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            error_flag_address(&d.err) != cudaSuccess) {
+            cudaGetLastError();
+            return GBN_ECUDA;
+        }
+        g_dev[dev] = d;
+        g_dev_ready[dev].store(1, std::memory_order_release);
+    }
+    *out = g_dev[dev];
+    return GBN_OK;
+}
+
+int elem_bytes(int dtype) { return dtype == GBN_F32 ? 4 : 2; }
+
+bool valid_dtype(int dtype) { return dtype == GBN_F32 || dtype == GBN_F16 || dtype == GBN_BF16; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Optional overrides for experiments: GBN_GRID forces G, GBN_WARPS_PER_ROW the slot width.
+int env_int(const char *name) {
+    const char *v = std::getenv(name);
+    return v ? std::atoi(v) : 0;
+}
+
+// Number of row blocks (CTAs) G: one per SM, more only when a block would
+// exceed kMaxRowsPerCta rows.  It depends on (M, SM count) only, so the
+// workspace size and the reduction order do not depend on buffer alignment.
+int grid_rows(int64_t M, const DevInfo &d) {
+    if (M <= 0) return 0;
+    int64_t G = d.sms;
+    const int forced = env_int("GBN_GRID");
+    if (forced > 0) G = forced;
+    if (G > M) G = M;
+    const int64_t min_g = (M + kMaxRowsPerCta - 1) / kMaxRowsPerCta;
+    if (G < min_g) G = min_g;
+    return static_cast<int>(G);
+}
+
+int partial_ld(int64_t N) { return static_cast<int>((N + 3) / 4 * 4); }
+
+struct StagedPlan {
+    bool ok = false;
+    int tpr = 0, nv = 0, stages = 0, stat_rows = 0;
+    size_t smem = 0;
+};
+
+// Launch shape of the bulk-copy staged kernels for rows of N elements, if
+// the row divides into 16-byte vectors and enough stages fit in shared memory.
+StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G, const DevInfo &d) {
+    StagedPlan P;
+    const int es = elem_bytes(dtype);
+    const int V = 16 / es;
+    if (N % V != 0) return P;
+    const int64_t nvec = N / V;
+    int W = 0;
+    const int forced = env_int("GBN_WARPS_PER_ROW");
+    if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16) {
+        if ((int64_t)32 * forced * kMaxVecPerThread >= nvec) W = forced;
+    }
+    if (!W) {
+        // smallest slot that covers the row with at most kMaxVecPerThread vectors
+        // per thread, and at least two vectors per thread when the row allows it
+        for (int w = 1; w <= kRingThreads / 32; w *= 2) {
+            if ((int64_t)32 * w * kMaxVecPerThread >= nvec) {
+                W = w;
+                break;
+            }
+        }
+    }
+    if (!W) return P;
+    P.tpr = 32 * W;
+    P.nv = static_cast<int>((nvec + P.tpr - 1) / P.tpr);
+    P.stat_rows = static_cast<int>((M + G - 1) / G);
+    const int slots = kRingThreads / P.tpr;
+    // as many stages as fit, at most 16 per slot
+    for (int S = 16; S >= 2; --S) {
+        const RingLayout L = ring_layout(bwd, ln, es, static_cast<int>(N), P.tpr, S, P.stat_rows, kRingThreads);
+        if (L.total <= static_cast<size_t>(d.smem_optin)) {
+            P.stages = S;
+            P.smem = L.total;
+            P.ok = true;
+            break;
+        }
+    }
+    (void)slots;
+    return P;
+}
+
+size_t workspace_bytes(int64_t M, int64_t N, bool ln, const DevInfo &d) {
+    const int G = grid_rows(M, d);
+    return (size_t)G * partial_ld(N) * 4 * (ln ? 2 : 1) + 256;
+}
+
+float *workspace_base(void *ws) {
+    const uintptr_t p = (reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255);
+    return reinterpret_cast<float *>(p);
+}
+
+int check_shape(int64_t M, int64_t N, int dtype) {
+    if (!valid_dtype(dtype)) return GBN_EDTYPE;
+    if (M < 0 || N < 1 || N > GBN_MAX_N) return GBN_EINVAL;
+    if (M > (int64_t(1) << 40)) return GBN_EINVAL;
+    return GBN_OK;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GBN_OK;
+    cudaGetLastError();
+    return GBN_ECUDA;
+}
+
+int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *y, float *mean, float *rstd,
+             float eps, int64_t M, int64_t N, int dtype, cudaStream_t stream) {
+    int st = check_shape(M, N, dtype);
+    if (st != GBN_OK) return st;
+    if (!(eps >= 0.f) || !isfinite(eps)) return GBN_EINVAL;
+    if (M == 0) return GBN_OK;
+    if (!x || !gamma || !y || !rstd || (ln && (!beta || !mean))) return GBN_EINVAL;
+    DevInfo d;
+    if ((st = device_info(&d)) != GBN_OK) return st;
+    FwdParams p{};
+    p.x = x; p.gamma = gamma; p.beta = beta; p.y = y; p.mean = mean; p.rstd = rstd; p.eps = eps;
+    p.M = M; p.N = static_cast<int>(N); p.G = grid_rows(M, d); p.err = d.err;
+    const bool aligned = aligned16(x) && aligned16(y) && aligned16(gamma) && (!ln || aligned16(beta));
+    StagedPlan P;
+    if (aligned) P = staged_plan(false, ln, dtype, M, N, p.G, d);
+    if (P.ok) {
+        p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
+        return cuda_status(launch_fwd_staged(dtype, ln, P.nv, p, P.smem, stream));
+    }
+    return cuda_status(launch_fwd_plain(dtype, ln, p, stream));
+}
+
+int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
+                  void *dx, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes_given,
+                  cudaStream_t stream) {
+    int st = check_shape(M, N, dtype);
+    if (st != GBN_OK) return st;
+    if (M == 0) return GBN_OK;
+    if (!dy || !x || !gamma || !rstd || !dx || !workspace || (ln && !mean)) return GBN_EINVAL;
+    DevInfo d;
+    if ((st = device_info(&d)) != GBN_OK) return st;
+    if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
+    BwdParams p{};
+    p.dy = dy; p.x = x; p.gamma = gamma; p.mean = mean; p.rstd = rstd; p.dx = dx;
+    p.part = workspace_base(workspace);
+    p.M = M; p.N = static_cast<int>(N); p.ldp = partial_ld(N); p.G = grid_rows(M, d); p.err = d.err;
+    const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma);
+    StagedPlan P;
+    if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
+    if (P.ok) {
+        p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
+        return cuda_status(launch_bwd_staged(dtype, ln, P.nv, p, P.smem, stream));
+    }
+    return cuda_status(launch_bwd_plain(dtype, ln, p, stream));
+}
+
+int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, int64_t N, int dtype, bool ln,
+                float *dgamma, float *dbeta, cudaStream_t stream) {
+    int st = check_shape(M, N, dtype);
+    if (st != GBN_OK) return st;
+    if (!dgamma || (ln && !dbeta)) return GBN_EINVAL;
+    if (M == 0) {
+        st = cuda_status(cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream));
+        if (st == GBN_OK && ln) st = cuda_status(cudaMemsetAsync(dbeta, 0, (size_t)N * 4, stream));
+        return st;
+    }
+    if (!workspace) return GBN_EINVAL;
+    DevInfo d;
+    if ((st = device_info(&d)) != GBN_OK) return st;
+    if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
+    const int G = grid_rows(M, d);
+    return cuda_status(launch_colsum(workspace_base(const_cast<void *>(workspace)), G, partial_ld(N),
+                                     static_cast<int>(N), dgamma, ln ? dbeta : nullptr, stream));
+}
+
+}  // namespace
+}  // namespace gbn
+
+using namespace gbn;
+
+extern "C" {
+
+size_t gbn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta) {
+    if (check_shape(M, N, dtype) != GBN_OK || M <= 0) return 0;
+    DevInfo d;
+    if (device_info(&d) != GBN_OK) return 0;
+    return workspace_bytes(M, N, has_beta != 0, d);
+}
+
+int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean, float *rstd, float eps,
+           int64_t M, int64_t N, int dtype, cudaStream_t stream) {
+    return fwd_impl(true, x, gamma, beta, y, mean, rstd, eps, M, N, dtype, stream);
+}
+
+int rms_fwd(const void *x, const void *gamma, void *y, float *rstd, float eps, int64_t M, int64_t N, int dtype,
+            cudaStream_t stream) {
+    return fwd_impl(false, x, gamma, nullptr, y, nullptr, rstd, eps, M, N, dtype, stream);
+}
+
+int ln_bwd_rows(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
+                int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
+}
+
+int rms_bwd_rows(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, int64_t M,
+                 int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
+}
+
+int gbn_bwd_reduce(const void *workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, int has_beta,
+                   float *dgamma, float *dbeta, cudaStream_t stream) {
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, has_beta != 0, dgamma, dbeta, stream);
+}
+
+int ln_bwd(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
+           float *dgamma, float *dbeta, float eps, int64_t M, int64_t N, int dtype, void *workspace,
+           size_t workspace_bytes, cudaStream_t stream) {
+    (void)eps;
+    if (M > 0 && (!dgamma || !dbeta)) return GBN_EINVAL;
+    int st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
+    if (st != GBN_OK) return st;
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, stream);
+}
+
+int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, float *dgamma, float eps,
+            int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    (void)eps;
+    if (M > 0 && !dgamma) return GBN_EINVAL;
+    int st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
+    if (st != GBN_OK) return st;
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, stream);
+}
+
+int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *staged) {
+    int st = check_shape(M, N, dtype);
+    if (st != GBN_OK) return st;
+    DevInfo d;
+    if ((st = device_info(&d)) != GBN_OK) return st;
+    const int g = grid_rows(M, d);
+    if (G) *G = g;
+    if (staged) *staged = M > 0 && staged_plan(true, has_beta != 0, dtype, M, N, g, d).ok ? 1 : 0;
+    return GBN_OK;
+}
+
+int gbn_device_error(int clear) {
+    int v = 0;
+    if (read_error_flag(&v, clear != 0) != cudaSuccess) {
+        cudaGetLastError();
+        return -GBN_ECUDA;
+    }
+    return v;
+}
+
+const char *gbn_status_string(int status) {
+    switch (status) {
+        case GBN_OK: return "ok";
+        case GBN_EINVAL: return "invalid argument (null pointer, bad M, N or eps)";
+        case GBN_EDTYPE: return "unknown dtype";
+        case GBN_EWORKSPACE: return "workspace smaller than gbn_bwd_workspace_bytes()";
+        case GBN_ECUDA: return "CUDA launch or query failed";
+        case GBN_EDEVICE: return "a kernel gave up on a bounded wait";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+"""The C-ABI library: it builds, loads, exports every symbol the header
+declares, and rejects bad arguments on the host (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbnorm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rmsnorm_backward_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("ln_fwd", "ln_bwd", "rms_fwd", "rms_bwd", "gbn_bwd_workspace_bytes", "gbn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libgbnorm.so does not export {name}"
+
+
+def test_status_strings(lib):
+    lib.gbn_status_string.restype = ctypes.c_char_p
+    lib.gbn_status_string.argtypes = [ctypes.c_int]
+    assert lib.gbn_status_string(0) == b"ok"
+    assert b"workspace" in lib.gbn_status_string(4)
+    assert lib.gbn_status_string(99) == b"unknown status"
+
+
+def test_host_side_argument_checks(lib):
+    import rmsnorm_backward_gb300 as gbn
+    L = gbn._declare(ctypes.CDLL(gbn.build.LIB if hasattr(gbn, "build") else gbn.library_path))
+    p = ctypes.c_void_p(16)
+    # null pointers with rows to process
+    assert L.ln_fwd(None, p, p, p, p, p, 1e-5, 4, 8, 2, None) == 1
+    assert L.rms_fwd(p, None, p, p, 1e-5, 4, 8, 2, None) == 1
+    assert L.rms_bwd(p, p, p, p, p, None, 0.0, 4, 8, 2, p, 1 << 20, None) == 1
+    assert L.ln_bwd(p, p, p, p, p, p, p, None, 0.0, 4, 8, 2, p, 1 << 20, None) == 1
+    # unknown dtype, bad sizes, bad eps
+    assert L.rms_fwd(p, p, p, p, 1e-5, 4, 8, 7, None) == 2
+    assert L.rms_fwd(p, p, p, p, 1e-5, -1, 8, 2, None) == 1
+    assert L.rms_fwd(p, p, p, p, 1e-5, 4, 0, 2, None) == 1
+    assert L.rms_fwd(p, p, p, p, -1.0, 4, 8, 2, None) == 1
+    assert L.rms_fwd(p, p, p, p, float("nan"), 4, 8, 2, None) == 1
+    assert L.rms_fwd(p, p, p, p, 1e-5, 4, (1 << 24) + 1, 2, None) == 1
+    # nothing to do
+    assert L.rms_fwd(None, None, None, None, 1e-5, 0, 8, 2, None) == 0
+    assert L.gbn_bwd_workspace_bytes(0, 8, 2, 0) == 0
+    assert L.gbn_bwd_workspace_bytes(4, 8, 9, 0) == 0
