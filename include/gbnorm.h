@@ -71,7 +71,8 @@ typedef enum {
     GBN_EDTYPE = 2,     /* dtype not one of gbn_dtype                         */
     GBN_EWORKSPACE = 4, /* workspace_bytes below gbn_bwd_workspace_bytes()    */
     GBN_ECUDA = 5,      /* a CUDA launch or query failed                      */
-    GBN_EDEVICE = 6     /* a kernel gave up on a bounded wait (see below)     */
+    GBN_EDEVICE = 6,    /* a kernel gave up on a bounded wait (see below)     */
+    GBN_ESCRATCH = 7    /* rms_bwd_noalloc: problem exceeds its static scratch */
 } gbn_status;
 
 /* Largest N accepted by every call. */
@@ -133,6 +134,36 @@ int ln_bwd(const void *dy, const void *x, const void *gamma, const float *mean,
 int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
             void *dx, float *dgamma, float eps, int64_t M, int64_t N, int dtype,
             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * rms_bwd_noalloc: rms_bwd for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it is a packaging of rms_bwd.
+ *
+ * Some callers cannot call cudaMalloc (or any allocating routine) where they
+ * run the backward: code inside an allocator's own callback, where
+ * allocating would re-enter the allocator; engines and plugins that run
+ * under a device-memory budget fixed up front and are handed no workspace;
+ * latency-critical loops that cannot afford the implicit device
+ * synchronisation a cudaMalloc / cudaFree may cause.  This call takes
+ * the same inputs and outputs as rms_bwd but no workspace: the per-CTA
+ * partial rows go to a static device array of GBN_NOALLOC_SCRATCH_BYTES
+ * that the library holds on every GPU that loads it, until the process
+ * exits.  It allocates nothing and frees nothing.
+ *   - Problems needing more than GBN_NOALLOC_SCRATCH_BYTES of workspace
+ *     (gbn_bwd_workspace_bytes(M, N, dtype, 0)) return GBN_ESCRATCH before
+ *     anything is enqueued.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last
+ *     call's partial rows; nothing in it needs clearing between calls.
+ *     Calls that overlap on the GPU (other streams, other threads) race on
+ *     it and give wrong dgamma: order them on one stream or with events.
+ */
+#define GBN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int rms_bwd_noalloc(const void *dy, const void *x, const void *gamma,
+                    const float *rstd, void *dx, float *dgamma, float eps,
+                    int64_t M, int64_t N, int dtype, cudaStream_t stream);
 
 /*
  * The two phases of the backward, for callers that time or overlap them

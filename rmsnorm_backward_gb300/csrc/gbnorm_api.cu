@@ -295,6 +295,7 @@ const char *gbn_status_string(int status) {
         case GBN_EWORKSPACE: return "workspace smaller than gbn_bwd_workspace_bytes()";
         case GBN_ECUDA: return "CUDA launch or query failed";
         case GBN_EDEVICE: return "a kernel gave up on a bounded wait";
+        case GBN_ESCRATCH: return "problem needs more workspace than rms_bwd_noalloc's static scratch holds";
     }
     return "unknown status";
 }
