@@ -175,6 +175,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// programmatic dependent launch: let the next kernel on the stream launch
+// now (it waits in griddep_wait until this grid has finished and its
+// memory is visible)
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // barrier over `count` threads (a multiple of 32) of this CTA, id in 1..15
 __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -87,16 +87,19 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     const int V = 16 / es;
     if (N % V != 0) return P;
     const int64_t nvec = N / V;
+    // Slot width W warps: the smallest that keeps a thread at <= 16 elements
+    // per row (values held in registers between the two passes); rows too
+    // wide for that take up to kMaxVecPerThread vectors per thread.
+    const int hold_vecs = 16 / V;
     int W = 0;
     const int forced = env_int("GBN_WARPS_PER_ROW");
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16) {
         if ((int64_t)32 * forced * kMaxVecPerThread >= nvec) W = forced;
     }
-    if (!W) {
-        // smallest slot that covers the row with at most kMaxVecPerThread vectors
-        // per thread, and at least two vectors per thread when the row allows it
+    for (int pass = 0; pass < 2 && !W; ++pass) {
+        const int cap = pass == 0 ? hold_vecs : kMaxVecPerThread;
         for (int w = 1; w <= kRingThreads / 32; w *= 2) {
-            if ((int64_t)32 * w * kMaxVecPerThread >= nvec) {
+            if ((int64_t)32 * w * cap >= nvec) {
                 W = w;
                 break;
             }

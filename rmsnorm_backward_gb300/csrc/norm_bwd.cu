@@ -33,10 +33,11 @@ namespace gbn {
 
 static __device__ int g_error_flag = 0;
 
-template <typename T, bool LN, int NV>
+template <typename T, bool LN, int NV, bool HOLD>
 __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdParams p) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
+    constexpr int E = NV * V;  // elements a thread owns per row
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int tid = threadIdx.x;
@@ -95,20 +96,27 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         st_rstd[i] = p.rstd[row0 + i];
         if (LN) st_mean[i] = p.mean[row0 + i];
     }
-    uint4 graw[NV];
+    // gamma: unpacked once (HOLD) or kept as raw vectors
+    float gam[HOLD ? E : 1];
+    uint4 graw[HOLD ? 1 : NV];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
         const int v = ts + j * tpr;
-        graw[j] = v < nvec ? ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V)
-                           : make_uint4(0, 0, 0, 0);
+        const uint4 g = v < nvec ? ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V)
+                                 : make_uint4(0, 0, 0, 0);
+        if constexpr (HOLD)
+            Tr::unpack(g, gam + j * V);
+        else
+            graw[j] = g;
     }
-    float acc_g[NV * V], acc_b[LN ? NV * V : 1];
+    float acc_g[E], acc_b[LN ? E : 1];
 #pragma unroll
-    for (int e = 0; e < NV * V; ++e) {
+    for (int e = 0; e < E; ++e) {
         acc_g[e] = 0.f;
         if constexpr (LN) acc_b[e] = 0.f;
     }
     __syncthreads();
+    griddep_launch_dependents();
 
     const float fn = static_cast<float>(N);
     int k = 0;
@@ -120,53 +128,69 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         const float rs = st_rstd[i];
         const float mu = LN ? st_mean[i] : 0.f;
         const unsigned char *sx = ring + (size_t)st * stage_bytes;
-        // pass 1 over the staged row: the two in-row sums and the per-column
-        // accumulators of dy*xhat and dy
+        // pass 1 over the staged row: the two in-row sums, the per-column
+        // accumulators of dy*xhat and dy, and (HOLD) xhat, dyhat kept in
+        // registers for pass 2
+        float xh[HOLD ? E : 1], dh[HOLD ? E : 1];
         float s[2] = {0.f, 0.f};  // sum(dyhat), sum(dyhat*xhat)
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int v = ts + j * tpr;
+            float xf[V], df[V], gl[V];
             if (v < nvec) {
-                float xf[V], df[V], gf[V];
                 Tr::unpack(*reinterpret_cast<const uint4 *>(sx + (size_t)v * 16), xf);
                 Tr::unpack(*reinterpret_cast<const uint4 *>(sx + rowb + (size_t)v * 16), df);
-                Tr::unpack(graw[j], gf);
+            } else {
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
-                    const float dyhat = df[e] * gf[e];
-                    if (LN) s[0] += dyhat;
-                    s[1] = fmaf(dyhat, xhat, s[1]);
-                    acc_g[j * V + e] = fmaf(df[e], xhat, acc_g[j * V + e]);
-                    if constexpr (LN) acc_b[j * V + e] += df[e];
+                for (int e = 0; e < V; ++e) xf[e] = df[e] = 0.f;
+            }
+            if constexpr (!HOLD) Tr::unpack(graw[j], gl);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const float g = HOLD ? gam[j * V + e] : gl[e];
+                const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
+                const float dyhat = df[e] * g;
+                if constexpr (LN) s[0] += dyhat;
+                s[1] = fmaf(dyhat, xhat, s[1]);
+                acc_g[j * V + e] = fmaf(df[e], xhat, acc_g[j * V + e]);
+                if constexpr (LN) acc_b[j * V + e] += df[e];
+                if constexpr (HOLD) {
+                    xh[j * V + e] = xhat;
+                    dh[j * V + e] = dyhat;
                 }
             }
         }
         const bool abort = slot_reduce<2>(s, red + (k & 1) * W * 2, flag, timed_out, W, warp, lane, 1 + slot, tpr);
         if (abort) break;
-        // every thread of the slot has finished pass 2 of the previous row:
-        // its stage can be refilled
-        if (ts == 0 && k > 0 && issued < ns) {
+        // HOLD: the slot is done with this stage; otherwise it re-reads this
+        // stage in pass 2 and the previous stage is the one now free
+        if (ts == 0 && issued < ns && (HOLD || k > 0)) {
             fence_proxy_async();
             issue(issued++);
         }
-        // pass 2: dx from the same staged row
-        const float c1 = LN ? s[0] / fn : 0.f;
-        const float c2 = s[1] / fn;
+        // pass 2: dx = rstd*(dyhat - c1 - xhat*c2) = dyhat*rstd + xhat*a + b
+        const float a = -rs * (s[1] / fn);
+        const float b = LN ? -rs * (s[0] / fn) : 0.f;
         T *dxrow = static_cast<T *>(p.dx) + (row0 + i) * N;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int v = ts + j * tpr;
             if (v < nvec) {
-                float xf[V], df[V], gf[V], o[V];
-                Tr::unpack(*reinterpret_cast<const uint4 *>(sx + (size_t)v * 16), xf);
-                Tr::unpack(*reinterpret_cast<const uint4 *>(sx + rowb + (size_t)v * 16), df);
-                Tr::unpack(graw[j], gf);
+                float o[V];
+                if constexpr (HOLD) {
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
-                    const float dyhat = df[e] * gf[e];
-                    o[e] = (dyhat - fmaf(xhat, c2, c1)) * rs;
+                    for (int e = 0; e < V; ++e)
+                        o[e] = fmaf(dh[j * V + e], rs, LN ? fmaf(xh[j * V + e], a, b) : xh[j * V + e] * a);
+                } else {
+                    float xf[V], df[V], gl[V];
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sx + (size_t)v * 16), xf);
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sx + rowb + (size_t)v * 16), df);
+                    Tr::unpack(graw[j], gl);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
+                        o[e] = fmaf(df[e] * gl[e], rs, LN ? fmaf(xhat, a, b) : xhat * a);
+                    }
                 }
                 st_global_cs_v4(dxrow + (size_t)v * V, Tr::pack(o));
             }
@@ -252,6 +276,7 @@ __global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdPar
     block_rows(p.M, p.G, blockIdx.x, row0, nrows);
     float *pg = p.part + (size_t)blockIdx.x * p.ldp;
     float *pb = p.part + ((size_t)p.G + blockIdx.x) * p.ldp;
+    griddep_launch_dependents();
     // column j is always handled by thread j % blockDim.x: a fixed order per column
     for (int j = threadIdx.x; j < N; j += blockDim.x) {
         pg[j] = 0.f;
@@ -286,33 +311,38 @@ __global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdPar
 }
 
 // dgamma[j] (blockIdx.y = 0) or dbeta[j] (blockIdx.y = 1) = sum over g of
-// part[g][j], g visited as slice, slice+8, ... then the 8 slices added in
-// order: a fixed order for every column.
-__global__ void __launch_bounds__(256) colsum_kernel(const float *__restrict__ part, int G, int ldp, int N,
-                                                     float *__restrict__ dgamma, float *__restrict__ dbeta) {
-    __shared__ float4 sm[8][32];
+// part[g][j].  Thread (slice, q) sums rows g = slice, slice + 16, ... of
+// column 32*blockIdx.x + q in that order (its loads issued together), then
+// the 16 slice sums are added in slice order: a fixed order per column.
+constexpr int kColsumSlices = 16;
+__global__ void __launch_bounds__(32 * kColsumSlices) colsum_kernel(const float *__restrict__ part, int G, int ldp,
+                                                                     int N, float *__restrict__ dgamma,
+                                                                     float *__restrict__ dbeta) {
+    __shared__ float sm[kColsumSlices][33];
+    griddep_wait();  // the partial rows of the kernel before this one
     const float *P = part + (size_t)blockIdx.y * G * ldp;
     float *out = blockIdx.y ? dbeta : dgamma;
     const int q = threadIdx.x & 31, slice = threadIdx.x >> 5;
-    const int c = (blockIdx.x * 32 + q) * 4;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c < ldp) {
-#pragma unroll 4
-        for (int g = slice; g < G; g += 8) {
-            const float4 b = __ldcg(reinterpret_cast<const float4 *>(P + (size_t)g * ldp + c));
-            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    const int c = blockIdx.x * 32 + q;
+    float a = 0.f;
+    if (c < N) {
+        for (int g0 = slice; g0 < G; g0 += kColsumSlices * 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int g = g0 + u * kColsumSlices;
+                v[u] = g < G ? __ldcg(P + (size_t)g * ldp + c) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a += v[u];
         }
     }
     sm[slice][q] = a;
     __syncthreads();
     if (slice == 0 && c < N) {
-        float4 t = sm[0][q];
-        for (int s = 1; s < 8; ++s) {
-            const float4 b = sm[s][q];
-            t.x += b.x; t.y += b.y; t.z += b.z; t.w += b.w;
-        }
-        const float v[4] = {t.x, t.y, t.z, t.w};
-        for (int e = 0; e < 4 && c + e < N; ++e) out[c + e] = v[e];
+        float t = sm[0][q];
+        for (int s2 = 1; s2 < kColsumSlices; ++s2) t += sm[s2][q];
+        out[c] = t;
     }
 }
 
@@ -321,7 +351,7 @@ __global__ void __launch_bounds__(256) colsum_kernel(const float *__restrict__ p
 // ---------------------------------------------------------------------------
 namespace {
 
-template <typename T, bool LN, int NV>
+template <typename T, bool LN, int NV, bool HOLD>
 cudaError_t bwd_staged_t(const BwdParams &p, size_t smem, cudaStream_t s) {
     static thread_local int set_for_dev = -1;
     int dev = 0;
@@ -331,21 +361,34 @@ cudaError_t bwd_staged_t(const BwdParams &p, size_t smem, cudaStream_t s) {
         int optin = 0;
         e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(bwd_staged_kernel<T, LN, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = cudaFuncSetAttribute(bwd_staged_kernel<T, LN, NV, HOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin);
         if (e != cudaSuccess) return e;
         set_for_dev = dev;
     }
-    bwd_staged_kernel<T, LN, NV><<<p.G, kRingThreads, smem, s>>>(p);
+    bwd_staged_kernel<T, LN, NV, HOLD><<<p.G, kRingThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
+// held-register variants cover up to 16 elements per thread; the re-read
+// variants the wider rows
 template <typename T, bool LN>
 cudaError_t bwd_staged_nv(int nv, const BwdParams &p, size_t smem, cudaStream_t s) {
-    switch (nv) {
-        case 1: return bwd_staged_t<T, LN, 1>(p, smem, s);
-        case 2: return bwd_staged_t<T, LN, 2>(p, smem, s);
-        case 3: return bwd_staged_t<T, LN, 3>(p, smem, s);
-        case 4: return bwd_staged_t<T, LN, 4>(p, smem, s);
+    constexpr int V = Traits<T>::kVec;
+    if (nv * V <= 16) {
+        switch (nv) {
+            case 1: return bwd_staged_t<T, LN, 1, true>(p, smem, s);
+            case 2: return bwd_staged_t<T, LN, 2, true>(p, smem, s);
+            case 3: if constexpr (3 * V <= 16) return bwd_staged_t<T, LN, 3, true>(p, smem, s); break;
+            case 4: if constexpr (4 * V <= 16) return bwd_staged_t<T, LN, 4, true>(p, smem, s); break;
+        }
+        return cudaErrorInvalidValue;
+    }
+    if constexpr (V == 8) {
+        switch (nv) {
+            case 3: return bwd_staged_t<T, LN, 3, false>(p, smem, s);
+            case 4: return bwd_staged_t<T, LN, 4, false>(p, smem, s);
+        }
     }
     return cudaErrorInvalidValue;
 }
@@ -385,10 +428,17 @@ cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_
 }
 
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, float *dgamma, float *dbeta, cudaStream_t s) {
-    const int cols4 = (ldp + 3) / 4;
-    dim3 grid((cols4 + 31) / 32, dbeta ? 2 : 1);
-    colsum_kernel<<<grid, 256, 0, s>>>(part, G, ldp, N, dgamma, dbeta);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + 31) / 32, dbeta ? 2 : 1);
+    cfg.blockDim = dim3(32 * kColsumSlices);
+    cfg.stream = s;
+    // launched as a programmatic dependent of the rows kernel before it
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, colsum_kernel, part, G, ldp, N, dgamma, dbeta);
 }
 
 cudaError_t error_flag_address(int **addr) {

@@ -21,10 +21,11 @@
 
 namespace gbn {
 
-template <typename T, bool LN, int NV>
+template <typename T, bool LN, int NV, bool HOLD>
 __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdParams p) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
+    constexpr int E = NV * V;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int tid = threadIdx.x;
@@ -72,18 +73,26 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
         for (; issued < S && issued < ns; ++issued) issue(issued);
     }
 
-    uint4 graw[NV], braw[NV];
+    // gamma / beta: unpacked once (HOLD) or kept as raw vectors
+    float gam[HOLD ? E : 1], bet[HOLD && LN ? E : 1];
+    uint4 graw[HOLD ? 1 : NV], braw[HOLD ? 1 : NV];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
         const int v = ts + j * tpr;
-        graw[j] = make_uint4(0, 0, 0, 0);
-        braw[j] = make_uint4(0, 0, 0, 0);
+        uint4 g = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
         if (v < nvec) {
-            graw[j] = ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V);
-            if (LN) braw[j] = ld_global_nc_v4(static_cast<const T *>(p.beta) + (size_t)v * V);
+            g = ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V);
+            if (LN) b = ld_global_nc_v4(static_cast<const T *>(p.beta) + (size_t)v * V);
+        }
+        if constexpr (HOLD) {
+            Tr::unpack(g, gam + j * V);
+            if constexpr (LN) Tr::unpack(b, bet + j * V);
+        } else {
+            graw[j] = g;
+            braw[j] = b;
         }
     }
-    const float inv_n_div = static_cast<float>(N);
+    const float fn = static_cast<float>(N);
 
     int k = 0;
     for (; k < ns; ++k) {
@@ -91,33 +100,43 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
         const bool timed_out = !mbar_wait_bounded(&bar[st], (k / S) & 1);
         if (timed_out) record_error(p.err, kErrWaitFull);
         const unsigned char *sx = ring + (size_t)st * rowb;
-        uint4 xr[NV];
+        // the row, in registers: fp32 values (HOLD) or raw vectors
+        float xf[HOLD ? E : 1];
+        uint4 xr[HOLD ? 1 : NV];
         float sum[1] = {0.f};
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int v = ts + j * tpr;
-            xr[j] = make_uint4(0, 0, 0, 0);
-            if (v < nvec) xr[j] = *reinterpret_cast<const uint4 *>(sx + (size_t)v * 16);
+            const uint4 raw = v < nvec ? *reinterpret_cast<const uint4 *>(sx + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
             float f[V];
-            Tr::unpack(xr[j], f);
+            Tr::unpack(raw, f);
 #pragma unroll
-            for (int e = 0; e < V; ++e) sum[0] = LN ? sum[0] + f[e] : fmaf(f[e], f[e], sum[0]);
+            for (int e = 0; e < V; ++e) {
+                sum[0] = LN ? sum[0] + f[e] : fmaf(f[e], f[e], sum[0]);
+                if constexpr (HOLD) xf[j * V + e] = f[e];
+            }
+            if constexpr (!HOLD) xr[j] = raw;
         }
-        // every thread of the slot now holds its part of the row in registers
-        bool abort = slot_reduce<1>(sum, red + (k & 1) * 2 * W * 2, flag, timed_out, W, warp, lane, 1 + slot, tpr);
+        const bool abort = slot_reduce<1>(sum, red + (k & 1) * 2 * W * 2, flag, timed_out, W, warp, lane, 1 + slot, tpr);
         if (abort) break;
+        // the slot has the row in registers: refill its stage
         if (ts == 0 && issued < ns) {
             fence_proxy_async();
             issue(issued++);
         }
         float mu = 0.f, rs;
-        if (LN) {
-            mu = sum[0] / inv_n_div;
+        if constexpr (LN) {
+            mu = sum[0] / fn;
             float sq[1] = {0.f};
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
                 float f[V];
-                Tr::unpack(xr[j], f);
+                if constexpr (HOLD) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) f[e] = xf[j * V + e];
+                } else {
+                    Tr::unpack(xr[j], f);
+                }
                 const bool live = ts + j * tpr < nvec;
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
@@ -126,9 +145,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
                 }
             }
             slot_reduce<1>(sq, red + ((k & 1) * 2 + 1) * W * 2, flag, false, W, warp, lane, 1 + slot, tpr);
-            rs = 1.0f / sqrtf(sq[0] / inv_n_div + p.eps);
+            rs = 1.0f / sqrtf(sq[0] / fn + p.eps);
         } else {
-            rs = 1.0f / sqrtf(sum[0] / inv_n_div + p.eps);
+            rs = 1.0f / sqrtf(sum[0] / fn + p.eps);
         }
         const int64_t row = row0 + slot + (int64_t)k * slots;
         T *yrow = static_cast<T *>(p.y) + row * N;
@@ -137,9 +156,18 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
             const int v = ts + j * tpr;
             if (v < nvec) {
                 float f[V], g[V], b[V], o[V];
-                Tr::unpack(xr[j], f);
-                Tr::unpack(graw[j], g);
-                if (LN) Tr::unpack(braw[j], b);
+                if constexpr (HOLD) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        f[e] = xf[j * V + e];
+                        g[e] = gam[j * V + e];
+                        b[e] = LN ? bet[j * V + e] : 0.f;
+                    }
+                } else {
+                    Tr::unpack(xr[j], f);
+                    Tr::unpack(graw[j], g);
+                    if constexpr (LN) Tr::unpack(braw[j], b);
+                }
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     const float xhat = LN ? (f[e] - mu) * rs : f[e] * rs;
@@ -217,27 +245,39 @@ cudaError_t allow_smem(K kernel) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
-template <typename T, bool LN, int NV>
+template <typename T, bool LN, int NV, bool HOLD>
 cudaError_t fwd_staged_t(const FwdParams &p, size_t smem, cudaStream_t s) {
     static thread_local int set_for_dev = -1;
     int dev = 0;
-    cudaGetDevice(&dev);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
     if (set_for_dev != dev) {
-        cudaError_t e = allow_smem(fwd_staged_kernel<T, LN, NV>);
+        e = allow_smem(fwd_staged_kernel<T, LN, NV, HOLD>);
         if (e != cudaSuccess) return e;
         set_for_dev = dev;
     }
-    fwd_staged_kernel<T, LN, NV><<<p.G, kRingThreads, smem, s>>>(p);
+    fwd_staged_kernel<T, LN, NV, HOLD><<<p.G, kRingThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
+// held-register variants up to 16 elements per thread, raw-vector ones beyond
 template <typename T, bool LN>
 cudaError_t fwd_staged_nv(int nv, const FwdParams &p, size_t smem, cudaStream_t s) {
-    switch (nv) {
-        case 1: return fwd_staged_t<T, LN, 1>(p, smem, s);
-        case 2: return fwd_staged_t<T, LN, 2>(p, smem, s);
-        case 3: return fwd_staged_t<T, LN, 3>(p, smem, s);
-        case 4: return fwd_staged_t<T, LN, 4>(p, smem, s);
+    constexpr int V = Traits<T>::kVec;
+    if (nv * V <= 16) {
+        switch (nv) {
+            case 1: return fwd_staged_t<T, LN, 1, true>(p, smem, s);
+            case 2: return fwd_staged_t<T, LN, 2, true>(p, smem, s);
+            case 3: if constexpr (3 * V <= 16) return fwd_staged_t<T, LN, 3, true>(p, smem, s); break;
+            case 4: if constexpr (4 * V <= 16) return fwd_staged_t<T, LN, 4, true>(p, smem, s); break;
+        }
+        return cudaErrorInvalidValue;
+    }
+    if constexpr (V == 8) {
+        switch (nv) {
+            case 3: return fwd_staged_t<T, LN, 3, false>(p, smem, s);
+            case 4: return fwd_staged_t<T, LN, 4, false>(p, smem, s);
+        }
     }
     return cudaErrorInvalidValue;
 }
