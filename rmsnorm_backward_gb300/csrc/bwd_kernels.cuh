@@ -1,0 +1,375 @@
+// bwd_kernels.cuh -- LayerNorm / RMSNorm backward kernel templates for
+// sm_103a, instantiated once per storage dtype in bwd_f32.cu, bwd_f16.cu and
+// bwd_bf16.cu.
+//
+// Definition followed: "Norm backward in Triton -- the dγ/dβ reduction",
+// section "The gradients": with dyhat = dy*gamma,
+//   dx = rstd*(dyhat - mean(dyhat) - xhat*mean(dyhat*xhat))   (RMSNorm: no
+//   mean(dyhat) term), dgamma = sum over rows of dy*xhat, dbeta = sum of dy.
+// xhat is recomputed from the saved per-row mean / rstd, never stored
+// ("Norm & activation backward", section "Half one").  dgamma / dbeta use the
+// disjoint-row-block scheme of "Norm backward in Triton", section "The hard
+// half": each CTA owns a contiguous block of rows, accumulates its partial
+// sums in registers and stores one partial row (no atomics); colsum_kernel
+// (norm_bwd.cu) then sums the partial rows per column in a fixed order.
+//
+// Kernels:
+//  * bwd_staged_kernel: one persistent CTA per SM; its rows are spread over
+//    slots of tpr threads.  Each slot streams x and dy rows through a ring of
+//    shared-memory stages filled by 1-D bulk (TMA) copies completing on
+//    mbarriers.  A thread owns NV fixed 16-byte column vectors.  Pass 1
+//    reads its vectors from the stage and forms the two in-row sums (warp
+//    shuffles plus one named barrier) and the per-column fp32 accumulators of
+//    dy*xhat and dy; pass 2 writes dx with 16-byte streaming stores, from
+//    xhat / dyhat held in registers (<= 16 elements per thread) or by
+//    re-reading the stage (wider rows).  The slot's barrier also shows that
+//    every thread is done with a stage, so the stage is refilled right away
+//    (held) or one row later (re-read).  At the end the slots' accumulators
+//    are added in slot order in shared memory and the CTA stores its
+//    partial row.
+//  * bwd_plain_kernel: any N and alignment, scalar loads, the CTA's own
+//    partial row in global memory as the accumulator.
+#pragma once
+
+#include <atomic>
+
+#include "gbn_device.cuh"
+#include "gbn_launch.h"
+
+namespace gbn {
+
+template <typename T, bool LN, int NV, bool FULL>
+__global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdParams p) {
+    using Tr = Traits<T>;
+    constexpr int V = Tr::kVec;
+    constexpr int E = NV * V;         // elements a thread owns per row
+    constexpr bool HOLD = E <= 16;    // xhat, dyhat kept in registers for pass 2
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x;
+    const int tpr = p.tpr;
+    const int slots = blockDim.x / tpr;
+    const int slot = tid / tpr;
+    const int ts = tid - slot * tpr;
+    const int W = tpr >> 5;
+    const int warp = ts >> 5;
+    const int lane = tid & 31;
+    const int N = p.N;
+    const int nvec = N / V;
+    const int S = p.stages;
+    const uint32_t rowb = static_cast<uint32_t>(N) * sizeof(T);
+    const uint32_t stage_bytes = 2 * rowb;
+    const uint32_t vstride = static_cast<uint32_t>(tpr) * 16;  // bytes between a thread's vectors
+
+    const RingLayout L = ring_layout(true, LN, sizeof(T), N, tpr, S, p.stat_rows, blockDim.x);
+    unsigned char *ring = smem + L.ring_off + (size_t)slot * S * stage_bytes;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bar_off) + slot * S;
+    float *st_rstd = reinterpret_cast<float *>(smem + L.stat_off);
+    float *st_mean = st_rstd + p.stat_rows;
+    float *red = reinterpret_cast<float *>(smem + L.red_off) + slot * 4 * 2 * kRedStride;
+    volatile int *flag = reinterpret_cast<int *>(smem + L.flag_off) + slot;
+
+    int64_t row0;
+    int nrows;
+    block_rows(p.M, p.G, blockIdx.x, row0, nrows);
+    const int ns = slot < nrows ? (nrows - slot + slots - 1) / slots : 0;
+
+    if (tid == 0) {
+        uint64_t *all = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+        for (int i = 0; i < slots * S; ++i) mbar_init(&all[i], 1);
+        fence_barrier_init();
+    }
+    if (ts == 0) *flag = 0;
+    __syncthreads();
+
+    // producer (thread 0 of the slot): the slot's rows in order
+    const uint64_t pol = policy_evict_first();
+    const size_t row_step = (size_t)slots * N;
+    const T *px = static_cast<const T *>(p.x) + (row0 + slot) * N;
+    const T *pdy = static_cast<const T *>(p.dy) + (row0 + slot) * N;
+    int issued = 0, pst = 0;
+    auto issue = [&]() {
+        unsigned char *dst = ring + (size_t)pst * stage_bytes;
+        mbar_arrive_expect_tx(&bar[pst], stage_bytes);
+        bulk_load(dst, px, rowb, &bar[pst], pol);
+        bulk_load(dst + rowb, pdy, rowb, &bar[pst], pol);
+        px += row_step;
+        pdy += row_step;
+        if (++pst == S) pst = 0;
+        ++issued;
+    };
+    if (ts == 0) {
+        while (issued < S && issued < ns) issue();
+    }
+
+    // this CTA's saved statistics, staged once
+    for (int i = tid; i < nrows; i += blockDim.x) {
+        st_rstd[i] = p.rstd[row0 + i];
+        if (LN) st_mean[i] = p.mean[row0 + i];
+    }
+    // gamma: unpacked once (HOLD) or kept as raw vectors
+    float gam[HOLD ? E : 1];
+    uint4 graw[HOLD ? 1 : NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int v = ts + j * tpr;
+        const uint4 g = (FULL || v < nvec) ? ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V)
+                                           : make_uint4(0, 0, 0, 0);
+        if constexpr (HOLD)
+            Tr::unpack(g, gam + j * V);
+        else
+            graw[j] = g;
+    }
+    float acc_g[E], acc_b[LN ? E : 1];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        acc_g[e] = 0.f;
+        if constexpr (LN) acc_b[e] = 0.f;
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+
+    const float inv_n = 1.0f / static_cast<float>(N);
+    T *dxrow = static_cast<T *>(p.dx) + (row0 + slot) * N + (size_t)ts * V;
+    RingPos pos;
+    int k = 0;
+    for (; k < ns; ++k) {
+        const bool timed_out = !mbar_wait_bounded(&bar[pos.stage], pos.parity);
+        if (timed_out) record_error(p.err, kErrWaitFull);
+        const int i = slot + k * slots;
+        const float rs = st_rstd[i];
+        const float mu = LN ? st_mean[i] : 0.f;
+        const unsigned char *sx = ring + (size_t)pos.stage * stage_bytes + (size_t)ts * 16;
+        const unsigned char *sdy = sx + rowb;
+        // pass 1
+        float xh[HOLD ? E : 1], dh[HOLD ? E : 1];
+        float s[2] = {0.f, 0.f};  // sum(dyhat), sum(dyhat*xhat)
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            float xf[V], df[V], gl[V];
+            if (FULL || ts + j * tpr < nvec) {
+                Tr::unpack(*reinterpret_cast<const uint4 *>(sx + j * vstride), xf);
+                Tr::unpack(*reinterpret_cast<const uint4 *>(sdy + j * vstride), df);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) xf[e] = df[e] = 0.f;
+            }
+            if constexpr (!HOLD) Tr::unpack(graw[j], gl);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const float g = HOLD ? gam[j * V + e] : gl[e];
+                const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
+                const float dyhat = df[e] * g;
+                if constexpr (LN) s[0] += dyhat;
+                s[1] = fmaf(dyhat, xhat, s[1]);
+                acc_g[j * V + e] = fmaf(df[e], xhat, acc_g[j * V + e]);
+                if constexpr (LN) acc_b[j * V + e] += df[e];
+                if constexpr (HOLD) {
+                    xh[j * V + e] = xhat;
+                    dh[j * V + e] = dyhat;
+                }
+            }
+        }
+        const bool abort = slot_reduce<2>(s, red + (k & 1) * 2 * kRedStride, flag, timed_out, W, warp, lane,
+                                          1 + slot, tpr);
+        if (abort) break;
+        // HOLD: the slot is done with this stage; otherwise it re-reads this
+        // stage in pass 2 and the previous stage is the one now free
+        if (ts == 0 && issued < ns && (HOLD || k > 0)) {
+            fence_proxy_async();
+            issue();
+        }
+        // pass 2: dx = rstd*(dyhat - c1 - xhat*c2) = dyhat*rstd + xhat*a + b
+        const float a = -rs * (s[1] * inv_n);
+        const float b = LN ? -rs * (s[0] * inv_n) : 0.f;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if (FULL || ts + j * tpr < nvec) {
+                float o[V];
+                if constexpr (HOLD) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e)
+                        o[e] = fmaf(dh[j * V + e], rs, LN ? fmaf(xh[j * V + e], a, b) : xh[j * V + e] * a);
+                } else {
+                    float xf[V], df[V], gl[V];
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sx + j * vstride), xf);
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sdy + j * vstride), df);
+                    Tr::unpack(graw[j], gl);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
+                        o[e] = fmaf(df[e] * gl[e], rs, LN ? fmaf(xhat, a, b) : xhat * a);
+                    }
+                }
+                st_global_cs_v4(dxrow + (size_t)j * tpr * V, Tr::pack(o));
+            }
+        }
+        dxrow += row_step;
+        pos.next(S);
+    }
+    // after a wait ran out: let the copies this slot still has in flight land
+    // (bounded) before the CTA exits
+    if (ts == 0) {
+        for (int kk = k; kk < issued; ++kk) {
+            if (!mbar_wait_bounded(&bar[kk % S], (kk / S) & 1, 100000000ull)) {
+                record_error(p.err, kErrDrain);
+                break;
+            }
+        }
+    }
+
+    // ---- this CTA's partial row(s) --------------------------------------
+    const int ldp = p.ldp;
+    float *pg = p.part + (size_t)blockIdx.x * ldp;
+    float *pb = p.part + ((size_t)p.G + blockIdx.x) * ldp;
+    if (slots == 1) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int v = ts + j * tpr;
+            if (FULL || v < nvec) {
+#pragma unroll
+                for (int e = 0; e < V; e += 4) {
+                    *reinterpret_cast<float4 *>(pg + (size_t)v * V + e) =
+                        make_float4(acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]);
+                    if constexpr (LN)
+                        *reinterpret_cast<float4 *>(pb + (size_t)v * V + e) = make_float4(
+                            acc_b[j * V + e], acc_b[j * V + e + 1], acc_b[j * V + e + 2], acc_b[j * V + e + 3]);
+                }
+            }
+        }
+        return;
+    }
+    // several slots: add their accumulators in slot order, in shared memory
+    __syncthreads();  // every slot is done with its ring stages
+    float *comb = reinterpret_cast<float *>(smem + L.ring_off);
+    float *comb_g = comb + (size_t)slot * ldp;
+    float *comb_b = comb + ((size_t)slots + slot) * ldp;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int v = ts + j * tpr;
+        if (FULL || v < nvec) {
+#pragma unroll
+            for (int e = 0; e < V; e += 4) {
+                *reinterpret_cast<float4 *>(comb_g + (size_t)v * V + e) =
+                    make_float4(acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]);
+                if constexpr (LN)
+                    *reinterpret_cast<float4 *>(comb_b + (size_t)v * V + e) =
+                        make_float4(acc_b[j * V + e], acc_b[j * V + e + 1], acc_b[j * V + e + 2], acc_b[j * V + e + 3]);
+            }
+        }
+    }
+    __syncthreads();
+    for (int c = tid * 4; c < N; c += blockDim.x * 4) {
+        float4 a = *reinterpret_cast<const float4 *>(comb + c);
+        for (int s2 = 1; s2 < slots; ++s2) {
+            const float4 b = *reinterpret_cast<const float4 *>(comb + (size_t)s2 * ldp + c);
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+        }
+        *reinterpret_cast<float4 *>(pg + c) = a;
+        if constexpr (LN) {
+            const float *cb = comb + (size_t)slots * ldp;
+            float4 d = *reinterpret_cast<const float4 *>(cb + c);
+            for (int s2 = 1; s2 < slots; ++s2) {
+                const float4 b = *reinterpret_cast<const float4 *>(cb + (size_t)s2 * ldp + c);
+                d.x += b.x; d.y += b.y; d.z += b.z; d.w += b.w;
+            }
+            *reinterpret_cast<float4 *>(pb + c) = d;
+        }
+    }
+}
+
+template <typename T, bool LN>
+__global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdParams p) {
+    using Tr = Traits<T>;
+    __shared__ float sm[kGenericThreads / 32];
+    const int N = p.N;
+    const float inv_n = 1.0f / static_cast<float>(N);
+    int64_t row0;
+    int nrows;
+    block_rows(p.M, p.G, blockIdx.x, row0, nrows);
+    float *pg = p.part + (size_t)blockIdx.x * p.ldp;
+    float *pb = p.part + ((size_t)p.G + blockIdx.x) * p.ldp;
+    griddep_launch_dependents();
+    // column j is always handled by thread j % blockDim.x: a fixed order per column
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        pg[j] = 0.f;
+        if (LN) pb[j] = 0.f;
+    }
+    const T *g = static_cast<const T *>(p.gamma);
+    for (int i = 0; i < nrows; ++i) {
+        const int64_t row = row0 + i;
+        const T *xr = static_cast<const T *>(p.x) + row * N;
+        const T *dyr = static_cast<const T *>(p.dy) + row * N;
+        const float rs = p.rstd[row];
+        const float mu = LN ? p.mean[row] : 0.f;
+        float s1 = 0.f, s2 = 0.f;
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const float xhat = (Tr::load1(xr + j) - mu) * rs;
+            const float dyhat = Tr::load1(dyr + j) * Tr::load1(g + j);
+            s1 += dyhat;
+            s2 = fmaf(dyhat, xhat, s2);
+        }
+        const float a = -rs * (block_sum(s2, sm) * inv_n);
+        const float b = LN ? -rs * (block_sum(s1, sm) * inv_n) : 0.f;
+        T *dxr = static_cast<T *>(p.dx) + row * N;
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const float xhat = (Tr::load1(xr + j) - mu) * rs;
+            const float dy = Tr::load1(dyr + j);
+            const float dyhat = dy * Tr::load1(g + j);
+            Tr::store1(dxr + j, fmaf(dyhat, rs, fmaf(xhat, a, b)));
+            pg[j] = fmaf(dy, xhat, pg[j]);
+            if (LN) pb[j] += dy;
+        }
+    }
+}
+
+// Sets the opt-in dynamic shared-memory limit of `kernel` once per device.
+template <typename K>
+cudaError_t ensure_smem_optin(K kernel, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && ((done.load(std::memory_order_acquire) >> dev) & 1u)) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess && dev < 64) done.fetch_or(uint64_t(1) << dev, std::memory_order_release);
+    return e;
+}
+
+template <typename T, bool LN, int NV, bool FULL>
+cudaError_t bwd_staged_launch(const BwdParams &p, size_t smem, cudaStream_t s) {
+    static std::atomic<uint64_t> done{0};
+    cudaError_t e = ensure_smem_optin(bwd_staged_kernel<T, LN, NV, FULL>, done);
+    if (e != cudaSuccess) return e;
+    bwd_staged_kernel<T, LN, NV, FULL><<<p.G, kRingThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, bool LN>
+cudaError_t bwd_staged_nv(int nv, bool full, const BwdParams &p, size_t smem, cudaStream_t s) {
+    switch (nv) {
+        case 1: return full ? bwd_staged_launch<T, LN, 1, true>(p, smem, s) : bwd_staged_launch<T, LN, 1, false>(p, smem, s);
+        case 2: return full ? bwd_staged_launch<T, LN, 2, true>(p, smem, s) : bwd_staged_launch<T, LN, 2, false>(p, smem, s);
+        case 3: return full ? bwd_staged_launch<T, LN, 3, true>(p, smem, s) : bwd_staged_launch<T, LN, 3, false>(p, smem, s);
+        case 4: return full ? bwd_staged_launch<T, LN, 4, true>(p, smem, s) : bwd_staged_launch<T, LN, 4, false>(p, smem, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t bwd_staged_dispatch(bool ln, int nv, bool full, const BwdParams &p, size_t smem, cudaStream_t s) {
+    return ln ? bwd_staged_nv<T, true>(nv, full, p, smem, s) : bwd_staged_nv<T, false>(nv, full, p, smem, s);
+}
+
+template <typename T>
+cudaError_t bwd_plain_dispatch(bool ln, const BwdParams &p, cudaStream_t s) {
+    if (ln)
+        bwd_plain_kernel<T, true><<<p.G, kGenericThreads, 0, s>>>(p);
+    else
+        bwd_plain_kernel<T, false><<<p.G, kGenericThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gbn

@@ -234,10 +234,14 @@ __host__ __device__ __forceinline__ void block_rows(int64_t M, int G, int b, int
 
 namespace gbn {
 
+// Floats of reduction scratch per slot and buffer: [NQ <= 2][16 warps].
+constexpr int kRedStride = 16;
+
 // Sums the NQ values of every thread of one row slot (W warps, tpr = 32*W
 // threads, named barrier bar_id) and leaves the totals in v on every thread
-// of the slot, summed warp by warp in a fixed order.  `buf` is this slot's
-// scratch of W*NQ floats; consecutive calls must alternate buffers.  Also
+// of the slot: a butterfly within each warp, then the W warp sums added in
+// warp order (read as 16-byte vectors).  `buf` is this slot's scratch of
+// NQ*kRedStride floats; consecutive calls must alternate buffers.  Also
 // returns, uniformly over the slot, whether any of its threads passed
 // give_up = true (a wait that ran out); `flag` is the slot's abort flag.
 template <int NQ>
@@ -249,17 +253,42 @@ __device__ __forceinline__ bool slot_reduce(float (&v)[NQ], float *buf, volatile
     if (give_up) *flag = 1;
     if (lane == 0) {
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) buf[warp * NQ + q] = v[q];
+        for (int q = 0; q < NQ; ++q) buf[q * kRedStride + warp] = v[q];
     }
     named_barrier(bar_id, tpr);
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
-        float s = buf[q];
-        for (int w = 1; w < W; ++w) s += buf[w * NQ + q];
-        v[q] = s;
+        const float *b = buf + q * kRedStride;
+        if (W == 2) {
+            const float2 t = *reinterpret_cast<const float2 *>(b);
+            v[q] = t.x + t.y;
+        } else {
+            float s = 0.f;
+            for (int w = 0; w < W; w += 4) {
+                const float4 t = *reinterpret_cast<const float4 *>(b + w);
+                s = w == 0 ? t.x : s + t.x;
+                s += t.y;
+                s += t.z;
+                s += t.w;
+            }
+            v[q] = s;
+        }
     }
     return *flag != 0;
 }
+
+// Stage ring position of one slot: stage index and the parity of the use of
+// that stage, advanced without division.
+struct RingPos {
+    int stage = 0;
+    uint32_t parity = 0;
+    __device__ __forceinline__ void next(int S) {
+        if (++stage == S) {
+            stage = 0;
+            parity ^= 1u;
+        }
+    }
+};
 
 // Block-wide sum for the plain-load kernels (blockDim.x = 32 * warps); every
 // thread gets the same bits.  `sm` holds one float per warp.

@@ -57,7 +57,7 @@ struct RingLayout {
     size_t ring_off, ring_bytes;  // [slots][stages][stage_bytes]; reused for the partial combine
     size_t bar_off;               // [slots][stages] mbarriers
     size_t stat_off;              // [stat_rows] rstd, then [stat_rows] mean (LayerNorm)
-    size_t red_off;               // [slots][4][warps per slot][2] floats
+    size_t red_off;               // [slots][4 buffers][2][kRedStride = 16] floats
     size_t flag_off;              // [slots] ints: per-slot abort flags
     size_t total;
 };
@@ -79,15 +79,18 @@ __host__ __device__ inline RingLayout ring_layout(bool bwd, bool ln, int es, int
     L.bar_off = L.ring_bytes;
     L.stat_off = L.bar_off + round_up((size_t)slots * stages * 8, 16);
     L.red_off = L.stat_off + round_up((size_t)stat_rows * 4 * (ln ? 2 : 1), 16);
-    L.flag_off = L.red_off + (size_t)slots * 4 * (tpr / 32) * 2 * 4;
+    L.flag_off = L.red_off + (size_t)slots * 4 * 2 * 16 * 4;
     L.total = round_up(L.flag_off + (size_t)slots * 4, 128);
     return L;
 }
 
 // dtype codes as in gbnorm.h
-cudaError_t launch_fwd_staged(int dtype, bool ln, int nv, const FwdParams &p, size_t smem, cudaStream_t s);
+// full: every thread's NV vectors lie inside the row (no bounds checks)
+cudaError_t launch_fwd_staged(int dtype, bool ln, int nv, bool full, const FwdParams &p, size_t smem,
+                              cudaStream_t s);
 cudaError_t launch_fwd_plain(int dtype, bool ln, const FwdParams &p, cudaStream_t s);
-cudaError_t launch_bwd_staged(int dtype, bool ln, int nv, const BwdParams &p, size_t smem, cudaStream_t s);
+cudaError_t launch_bwd_staged(int dtype, bool ln, int nv, bool full, const BwdParams &p, size_t smem,
+                              cudaStream_t s);
 cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_t s);
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, float *dgamma, float *dbeta,
                           cudaStream_t s);

@@ -75,6 +75,7 @@ int partial_ld(int64_t N) { return static_cast<int>((N + 3) / 4 * 4); }
 
 struct StagedPlan {
     bool ok = false;
+    bool full = false;  // nv * tpr vectors exactly cover the row
     int tpr = 0, nv = 0, stages = 0, stat_rows = 0;
     size_t smem = 0;
 };
@@ -87,10 +88,12 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     const int V = 16 / es;
     if (N % V != 0) return P;
     const int64_t nvec = N / V;
-    // Slot width W warps: the smallest that keeps a thread at <= 16 elements
-    // per row (values held in registers between the two passes); rows too
-    // wide for that take up to kMaxVecPerThread vectors per thread.
-    const int hold_vecs = 16 / V;
+    // Slot width W warps.  Backward: the smallest that keeps a thread at
+    // <= 16 elements per row (xhat, dyhat held in registers between the two
+    // passes), else up to kMaxVecPerThread vectors.  Forward: the smallest
+    // with up to kMaxVecPerThread vectors per thread (more rows in flight
+    // per CTA measured faster than fewer elements per thread).
+    const int hold_vecs = bwd ? 16 / V : kMaxVecPerThread;
     int W = 0;
     const int forced = env_int("GBN_WARPS_PER_ROW");
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16) {
@@ -108,6 +111,7 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     if (!W) return P;
     P.tpr = 32 * W;
     P.nv = static_cast<int>((nvec + P.tpr - 1) / P.tpr);
+    P.full = (int64_t)P.nv * P.tpr == nvec;
     P.stat_rows = static_cast<int>((M + G - 1) / G);
     const int slots = kRingThreads / P.tpr;
     // as many stages as fit, at most 16 per slot
@@ -164,7 +168,7 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
     if (aligned) P = staged_plan(false, ln, dtype, M, N, p.G, d);
     if (P.ok) {
         p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
-        return cuda_status(launch_fwd_staged(dtype, ln, P.nv, p, P.smem, stream));
+        return cuda_status(launch_fwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
     }
     return cuda_status(launch_fwd_plain(dtype, ln, p, stream));
 }
@@ -188,7 +192,7 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
     if (P.ok) {
         p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
-        return cuda_status(launch_bwd_staged(dtype, ln, P.nv, p, P.smem, stream));
+        return cuda_status(launch_bwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
     }
     return cuda_status(launch_bwd_plain(dtype, ln, p, stream));
 }
