@@ -21,8 +21,9 @@
 //    reads its vectors from the stage and forms the two in-row sums (warp
 //    shuffles plus one named barrier) and the per-column fp32 accumulators of
 //    dy*xhat and dy; pass 2 writes dx with 16-byte streaming stores, from
-//    xhat / dyhat held in registers (<= 16 elements per thread) or by
-//    re-reading the stage (wider rows).  The slot's barrier also shows that
+//    values held in registers (xhat and dyhat up to 16 elements per thread;
+//    raw x and dyhat up to 32 for RMSNorm, gamma then staged in shared
+//    memory) or by re-reading the stage (wider rows).  The slot's barrier also shows that
 //    every thread is done with a stage, so the stage is refilled right away
 //    (held) or one row later (re-read).  At the end the slots' accumulators
 //    are added in slot order in shared memory and the CTA stores its
@@ -42,8 +43,10 @@ template <typename T, bool LN, int NV, bool FULL>
 __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdParams p) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
-    constexpr int E = NV * V;         // elements a thread owns per row
-    constexpr bool HOLD = E <= 16;    // xhat, dyhat kept in registers for pass 2
+    constexpr int E = NV * V;                         // elements a thread owns per row
+    constexpr int MODE = bwd_hold_mode(LN, E);        // what pass 2 finds in registers
+    constexpr bool HOLD = MODE != kReread;            // the stage is free after pass 1
+    constexpr bool GSMEM = bwd_gamma_smem(LN, E);     // gamma read from shared memory (fp32)
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int tid = threadIdx.x;
@@ -61,9 +64,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     const uint32_t stage_bytes = 2 * rowb;
     const uint32_t vstride = static_cast<uint32_t>(tpr) * 16;  // bytes between a thread's vectors
 
-    const RingLayout L = ring_layout(true, LN, sizeof(T), N, tpr, S, p.stat_rows, blockDim.x);
+    const RingLayout L = ring_layout(true, LN, sizeof(T), N, tpr, S, p.stat_rows, blockDim.x, GSMEM);
     unsigned char *ring = smem + L.ring_off + (size_t)slot * S * stage_bytes;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bar_off) + slot * S;
+    float *gam_s = reinterpret_cast<float *>(smem + L.gam_off);
     float *st_rstd = reinterpret_cast<float *>(smem + L.stat_off);
     float *st_mean = st_rstd + p.stat_rows;
     float *red = reinterpret_cast<float *>(smem + L.red_off) + slot * 4 * 2 * kRedStride;
@@ -83,18 +87,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     __syncthreads();
 
     // producer (thread 0 of the slot): the slot's rows in order
-    const uint64_t pol = policy_evict_first();
     const size_t row_step = (size_t)slots * N;
-    const T *px = static_cast<const T *>(p.x) + (row0 + slot) * N;
-    const T *pdy = static_cast<const T *>(p.dy) + (row0 + slot) * N;
     int issued = 0, pst = 0;
     auto issue = [&]() {
+        const size_t off = (size_t)(row0 + slot + (int64_t)issued * slots) * N;
+        const uint64_t pol = policy_evict_first();
         unsigned char *dst = ring + (size_t)pst * stage_bytes;
         mbar_arrive_expect_tx(&bar[pst], stage_bytes);
-        bulk_load(dst, px, rowb, &bar[pst], pol);
-        bulk_load(dst + rowb, pdy, rowb, &bar[pst], pol);
-        px += row_step;
-        pdy += row_step;
+        bulk_load(dst, static_cast<const T *>(p.x) + off, rowb, &bar[pst], pol);
+        bulk_load(dst + rowb, static_cast<const T *>(p.dy) + off, rowb, &bar[pst], pol);
         if (++pst == S) pst = 0;
         ++issued;
     };
@@ -107,18 +108,30 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         st_rstd[i] = p.rstd[row0 + i];
         if (LN) st_mean[i] = p.mean[row0 + i];
     }
-    // gamma: unpacked once (HOLD) or kept as raw vectors
-    float gam[HOLD ? E : 1];
+    // gamma: unpacked into registers (kHoldAll), unpacked into shared memory
+    // (kHoldX), or kept as raw vectors (kReread)
+    constexpr bool GREG = HOLD && !GSMEM;
+    float gam[GREG ? E : 1];
     uint4 graw[HOLD ? 1 : NV];
+    if constexpr (GSMEM) {
+        for (int v = tid; v < nvec; v += blockDim.x) {
+            float f[V];
+            Tr::unpack(ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V), f);
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        const int v = ts + j * tpr;
-        const uint4 g = (FULL || v < nvec) ? ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V)
-                                           : make_uint4(0, 0, 0, 0);
-        if constexpr (HOLD)
-            Tr::unpack(g, gam + j * V);
-        else
-            graw[j] = g;
+            for (int e = 0; e < V; e += 4)
+                *reinterpret_cast<float4 *>(gam_s + (size_t)v * V + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int v = ts + j * tpr;
+            const uint4 g = (FULL || v < nvec) ? ld_global_nc_v4(static_cast<const T *>(p.gamma) + (size_t)v * V)
+                                               : make_uint4(0, 0, 0, 0);
+            if constexpr (GREG)
+                Tr::unpack(g, gam + j * V);
+            else
+                graw[j] = g;
+        }
     }
     float acc_g[E], acc_b[LN ? E : 1];
 #pragma unroll
@@ -142,32 +155,43 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         const unsigned char *sx = ring + (size_t)pos.stage * stage_bytes + (size_t)ts * 16;
         const unsigned char *sdy = sx + rowb;
         // pass 1
-        float xh[HOLD ? E : 1], dh[HOLD ? E : 1];
+        float xh[MODE == kHoldAll ? E : 1], dh[HOLD ? E : 1];
+        uint4 xraw[MODE == kHoldX ? NV : 1];
         float s[2] = {0.f, 0.f};  // sum(dyhat), sum(dyhat*xhat)
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             float xf[V], df[V], gl[V];
             if (FULL || ts + j * tpr < nvec) {
-                Tr::unpack(*reinterpret_cast<const uint4 *>(sx + j * vstride), xf);
+                const uint4 xv = *reinterpret_cast<const uint4 *>(sx + j * vstride);
+                if constexpr (MODE == kHoldX) xraw[j] = xv;
+                Tr::unpack(xv, xf);
                 Tr::unpack(*reinterpret_cast<const uint4 *>(sdy + j * vstride), df);
             } else {
+                if constexpr (MODE == kHoldX) xraw[j] = make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int e = 0; e < V; ++e) xf[e] = df[e] = 0.f;
             }
             if constexpr (!HOLD) Tr::unpack(graw[j], gl);
+            if constexpr (GSMEM) {
+                const float *gs = gam_s + (size_t)(ts + j * tpr) * V;
+#pragma unroll
+                for (int e = 0; e < V; e += 4) {
+                    const float4 t = (FULL || ts + j * tpr < nvec) ? *reinterpret_cast<const float4 *>(gs + e)
+                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    gl[e] = t.x; gl[e + 1] = t.y; gl[e + 2] = t.z; gl[e + 3] = t.w;
+                }
+            }
 #pragma unroll
             for (int e = 0; e < V; ++e) {
-                const float g = HOLD ? gam[j * V + e] : gl[e];
+                const float g = GREG ? gam[j * V + e] : gl[e];
                 const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
                 const float dyhat = df[e] * g;
                 if constexpr (LN) s[0] += dyhat;
                 s[1] = fmaf(dyhat, xhat, s[1]);
                 acc_g[j * V + e] = fmaf(df[e], xhat, acc_g[j * V + e]);
                 if constexpr (LN) acc_b[j * V + e] += df[e];
-                if constexpr (HOLD) {
-                    xh[j * V + e] = xhat;
-                    dh[j * V + e] = dyhat;
-                }
+                if constexpr (MODE == kHoldAll) xh[j * V + e] = xhat;
+                if constexpr (HOLD) dh[j * V + e] = dyhat;
             }
         }
         const bool abort = slot_reduce<2>(s, red + (k & 1) * 2 * kRedStride, flag, timed_out, W, warp, lane,
@@ -182,14 +206,20 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         // pass 2: dx = rstd*(dyhat - c1 - xhat*c2) = dyhat*rstd + xhat*a + b
         const float a = -rs * (s[1] * inv_n);
         const float b = LN ? -rs * (s[0] * inv_n) : 0.f;
+        const float ax = a * rs;  // kHoldX (RMSNorm): xhat*a = x*(rstd*a)
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             if (FULL || ts + j * tpr < nvec) {
                 float o[V];
-                if constexpr (HOLD) {
+                if constexpr (MODE == kHoldAll) {
 #pragma unroll
                     for (int e = 0; e < V; ++e)
                         o[e] = fmaf(dh[j * V + e], rs, LN ? fmaf(xh[j * V + e], a, b) : xh[j * V + e] * a);
+                } else if constexpr (MODE == kHoldX) {
+                    float xf[V];
+                    Tr::unpack(xraw[j], xf);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) o[e] = fmaf(dh[j * V + e], rs, xf[e] * ax);
                 } else {
                     float xf[V], df[V], gl[V];
                     Tr::unpack(*reinterpret_cast<const uint4 *>(sx + j * vstride), xf);

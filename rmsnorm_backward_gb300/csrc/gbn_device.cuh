@@ -244,11 +244,31 @@ constexpr int kRedStride = 16;
 // NQ*kRedStride floats; consecutive calls must alternate buffers.  Also
 // returns, uniformly over the slot, whether any of its threads passed
 // give_up = true (a wait that ran out); `flag` is the slot's abort flag.
+// Butterfly sum of two values over the 32 lanes with six shuffles: after the
+// first exchange, lanes 0-15 carry partial sums of v0 and lanes 16-31 of v1;
+// four more butterfly steps finish both (each half's lanes end with the same
+// bits), and a last exchange gives every lane both totals.
+__device__ __forceinline__ void warp_sum2(float &v0, float &v1) {
+    const bool hi = (threadIdx.x & 16) != 0;
+    const float send = hi ? v0 : v1;
+    const float keep = hi ? v1 : v0;
+    float t = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const float other = __shfl_xor_sync(0xffffffffu, t, 16);
+    v0 = hi ? other : t;
+    v1 = hi ? t : other;
+}
+
 template <int NQ>
 __device__ __forceinline__ bool slot_reduce(float (&v)[NQ], float *buf, volatile int *flag, bool give_up,
                                             int W, int warp, int lane, int bar_id, int tpr) {
+    if constexpr (NQ == 2) {
+        warp_sum2(v[0], v[1]);
+    } else {
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) v[q] = warp_sum(v[q]);
+        for (int q = 0; q < NQ; ++q) v[q] = warp_sum(v[q]);
+    }
     if (W == 1) return __any_sync(0xffffffffu, give_up) != 0;
     if (give_up) *flag = 1;
     if (lane == 0) {

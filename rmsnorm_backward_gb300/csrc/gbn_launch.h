@@ -55,6 +55,7 @@ struct BwdParams {
 // host (to size the launch) and on the device (to carve the buffer).
 struct RingLayout {
     size_t ring_off, ring_bytes;  // [slots][stages][stage_bytes]; reused for the partial combine
+    size_t gam_off;               // [N] fp32 gamma (backward kernels that stage it), else empty
     size_t bar_off;               // [slots][stages] mbarriers
     size_t stat_off;              // [stat_rows] rstd, then [stat_rows] mean (LayerNorm)
     size_t red_off;               // [slots][4 buffers][2][kRedStride = 16] floats
@@ -64,8 +65,20 @@ struct RingLayout {
 
 __host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// What the staged backward keeps in registers between its two passes, for a
+// thread that owns `elems` elements of a row:
+//   kHoldAll: xhat and dyhat in fp32 (up to 16 elements), gamma in registers;
+//   kHoldX:   x as raw 16-byte vectors and dyhat in fp32 (RMSNorm, up to 32
+//             elements), gamma unpacked once into shared memory;
+//   kReread:  nothing; pass 2 re-reads the staged row.
+enum BwdHold : int { kHoldAll = 0, kHoldX = 1, kReread = 2 };
+__host__ __device__ constexpr int bwd_hold_mode(bool ln, int elems) {
+    return elems <= 16 ? kHoldAll : (!ln && elems <= 32 ? kHoldX : kReread);
+}
+__host__ __device__ constexpr bool bwd_gamma_smem(bool ln, int elems) { return bwd_hold_mode(ln, elems) == kHoldX; }
+
 __host__ __device__ inline RingLayout ring_layout(bool bwd, bool ln, int es, int N, int tpr, int stages,
-                                                  int stat_rows, int threads) {
+                                                  int stat_rows, int threads, bool gamma_smem = false) {
     RingLayout L;
     const int slots = threads / tpr;
     const size_t stage_bytes = (bwd ? 2u : 1u) * (size_t)N * es;
@@ -76,7 +89,8 @@ __host__ __device__ inline RingLayout ring_layout(bool bwd, bool ln, int es, int
     }
     L.ring_off = 0;
     L.ring_bytes = round_up(ring, 128);
-    L.bar_off = L.ring_bytes;
+    L.gam_off = L.ring_bytes;
+    L.bar_off = L.gam_off + (gamma_smem ? round_up((size_t)N * 4, 128) : 0);
     L.stat_off = L.bar_off + round_up((size_t)slots * stages * 8, 16);
     L.red_off = L.stat_off + round_up((size_t)stat_rows * 4 * (ln ? 2 : 1), 16);
     L.flag_off = L.red_off + (size_t)slots * 4 * 2 * 16 * 4;

@@ -51,7 +51,8 @@ bool valid_dtype(int dtype) { return dtype == GBN_F32 || dtype == GBN_F16 || dty
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Optional overrides for experiments: GBN_GRID forces G, GBN_WARPS_PER_ROW the slot width.
+// Optional overrides for experiments: GBN_GRID forces G, GBN_WARPS_PER_ROW the
+// slot width, GBN_NO_FULL=1 the bounds-checked kernel variants.
 int env_int(const char *name) {
     const char *v = std::getenv(name);
     return v ? std::atoi(v) : 0;
@@ -88,12 +89,14 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     const int V = 16 / es;
     if (N % V != 0) return P;
     const int64_t nvec = N / V;
-    // Slot width W warps.  Backward: the smallest that keeps a thread at
-    // <= 16 elements per row (xhat, dyhat held in registers between the two
-    // passes), else up to kMaxVecPerThread vectors.  Forward: the smallest
-    // with up to kMaxVecPerThread vectors per thread (more rows in flight
-    // per CTA measured faster than fewer elements per thread).
-    const int hold_vecs = bwd ? 16 / V : kMaxVecPerThread;
+    // Slot width W warps.  Backward: the smallest that keeps a thread within
+    // the elements it can hold in registers between the two passes (16 for
+    // LayerNorm, 32 for RMSNorm), else up to kMaxVecPerThread vectors.
+    // Forward: the smallest with up to kMaxVecPerThread vectors per thread.
+    // (More rows in flight per CTA measured faster than fewer elements per
+    // thread.)
+    const int hold_elems = ln ? 16 : 32;
+    const int hold_vecs = bwd && hold_elems / V < kMaxVecPerThread ? hold_elems / V : kMaxVecPerThread;
     int W = 0;
     const int forced = env_int("GBN_WARPS_PER_ROW");
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16) {
@@ -111,12 +114,16 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     if (!W) return P;
     P.tpr = 32 * W;
     P.nv = static_cast<int>((nvec + P.tpr - 1) / P.tpr);
-    P.full = (int64_t)P.nv * P.tpr == nvec;
+    // exact tiling drops the bounds checks, except in the x-holding backward
+    // mode, where the unchecked variant measured slower (register spills)
+    P.full = (int64_t)P.nv * P.tpr == nvec && env_int("GBN_NO_FULL") == 0 &&
+             !(bwd && bwd_hold_mode(ln, P.nv * V) == kHoldX);
     P.stat_rows = static_cast<int>((M + G - 1) / G);
     const int slots = kRingThreads / P.tpr;
     // as many stages as fit, at most 16 per slot
     for (int S = 16; S >= 2; --S) {
-        const RingLayout L = ring_layout(bwd, ln, es, static_cast<int>(N), P.tpr, S, P.stat_rows, kRingThreads);
+        const RingLayout L = ring_layout(bwd, ln, es, static_cast<int>(N), P.tpr, S, P.stat_rows, kRingThreads,
+                                         bwd && bwd_gamma_smem(ln, P.nv * V));
         if (L.total <= static_cast<size_t>(d.smem_optin)) {
             P.stages = S;
             P.smem = L.total;
