@@ -96,10 +96,14 @@ def measured_hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of every CUDA source of the library (a traffic record taken from
+    an ncu capture is only valid for the sources it was captured from)."""
+    import glob
+
     h = hashlib.sha256()
-    for rel in ("rmsnorm_backward_gb300/csrc/norm_bwd.cu", "rmsnorm_backward_gb300/csrc/gbn_device.cuh",
-                "rmsnorm_backward_gb300/csrc/gbn_launch.h", "rmsnorm_backward_gb300/csrc/gbnorm_api.cu"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
+    for path in sorted(glob.glob(os.path.join(ROOT, "rmsnorm_backward_gb300", "csrc", "*"))):
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 

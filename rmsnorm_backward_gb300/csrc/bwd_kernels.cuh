@@ -91,11 +91,16 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     int issued = 0, pst = 0;
     auto issue = [&]() {
         const size_t off = (size_t)(row0 + slot + (int64_t)issued * slots) * N;
-        const uint64_t pol = policy_evict_first();
         unsigned char *dst = ring + (size_t)pst * stage_bytes;
         mbar_arrive_expect_tx(&bar[pst], stage_bytes);
-        bulk_load(dst, static_cast<const T *>(p.x) + off, rowb, &bar[pst], pol);
-        bulk_load(dst + rowb, static_cast<const T *>(p.dy) + off, rowb, &bar[pst], pol);
+        if (p.l2_hint) {
+            const uint64_t pol = policy_evict_first();
+            bulk_load(dst, static_cast<const T *>(p.x) + off, rowb, &bar[pst], pol);
+            bulk_load(dst + rowb, static_cast<const T *>(p.dy) + off, rowb, &bar[pst], pol);
+        } else {
+            bulk_load_nohint(dst, static_cast<const T *>(p.x) + off, rowb, &bar[pst]);
+            bulk_load_nohint(dst + rowb, static_cast<const T *>(p.dy) + off, rowb, &bar[pst]);
+        }
         if (++pst == S) pst = 0;
         ++issued;
     };
@@ -267,43 +272,43 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
                 }
             }
         }
-        return;
-    }
-    // several slots: add their accumulators in slot order, in shared memory
-    __syncthreads();  // every slot is done with its ring stages
-    float *comb = reinterpret_cast<float *>(smem + L.ring_off);
-    float *comb_g = comb + (size_t)slot * ldp;
-    float *comb_b = comb + ((size_t)slots + slot) * ldp;
+    } else {
+        // several slots: add their accumulators in slot order, in shared memory
+        __syncthreads();  // every slot is done with its ring stages
+        float *comb = reinterpret_cast<float *>(smem + L.ring_off);
+        float *comb_g = comb + (size_t)slot * ldp;
+        float *comb_b = comb + ((size_t)slots + slot) * ldp;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        const int v = ts + j * tpr;
-        if (FULL || v < nvec) {
+        for (int j = 0; j < NV; ++j) {
+            const int v = ts + j * tpr;
+            if (FULL || v < nvec) {
 #pragma unroll
-            for (int e = 0; e < V; e += 4) {
-                *reinterpret_cast<float4 *>(comb_g + (size_t)v * V + e) =
-                    make_float4(acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]);
-                if constexpr (LN)
-                    *reinterpret_cast<float4 *>(comb_b + (size_t)v * V + e) =
-                        make_float4(acc_b[j * V + e], acc_b[j * V + e + 1], acc_b[j * V + e + 2], acc_b[j * V + e + 3]);
+                for (int e = 0; e < V; e += 4) {
+                    *reinterpret_cast<float4 *>(comb_g + (size_t)v * V + e) = make_float4(
+                        acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]);
+                    if constexpr (LN)
+                        *reinterpret_cast<float4 *>(comb_b + (size_t)v * V + e) = make_float4(
+                            acc_b[j * V + e], acc_b[j * V + e + 1], acc_b[j * V + e + 2], acc_b[j * V + e + 3]);
+                }
             }
         }
-    }
-    __syncthreads();
-    for (int c = tid * 4; c < N; c += blockDim.x * 4) {
-        float4 a = *reinterpret_cast<const float4 *>(comb + c);
-        for (int s2 = 1; s2 < slots; ++s2) {
-            const float4 b = *reinterpret_cast<const float4 *>(comb + (size_t)s2 * ldp + c);
-            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-        }
-        *reinterpret_cast<float4 *>(pg + c) = a;
-        if constexpr (LN) {
-            const float *cb = comb + (size_t)slots * ldp;
-            float4 d = *reinterpret_cast<const float4 *>(cb + c);
+        __syncthreads();
+        for (int c = tid * 4; c < N; c += blockDim.x * 4) {
+            float4 a = *reinterpret_cast<const float4 *>(comb + c);
             for (int s2 = 1; s2 < slots; ++s2) {
-                const float4 b = *reinterpret_cast<const float4 *>(cb + (size_t)s2 * ldp + c);
-                d.x += b.x; d.y += b.y; d.z += b.z; d.w += b.w;
+                const float4 b = *reinterpret_cast<const float4 *>(comb + (size_t)s2 * ldp + c);
+                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
             }
-            *reinterpret_cast<float4 *>(pb + c) = d;
+            *reinterpret_cast<float4 *>(pg + c) = a;
+            if constexpr (LN) {
+                const float *cb = comb + (size_t)slots * ldp;
+                float4 d = *reinterpret_cast<const float4 *>(cb + c);
+                for (int s2 = 1; s2 < slots; ++s2) {
+                    const float4 b = *reinterpret_cast<const float4 *>(cb + (size_t)s2 * ldp + c);
+                    d.x += b.x; d.y += b.y; d.z += b.z; d.w += b.w;
+                }
+                *reinterpret_cast<float4 *>(pb + c) = d;
+            }
         }
     }
 }

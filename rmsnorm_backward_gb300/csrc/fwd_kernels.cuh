@@ -76,7 +76,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
     int issued = 0, pst = 0;
     auto issue = [&]() {
         mbar_arrive_expect_tx(&bar[pst], rowb);
-        bulk_load(ring + (size_t)pst * rowb, px, rowb, &bar[pst], pol);
+        if (p.l2_hint)
+            bulk_load(ring + (size_t)pst * rowb, px, rowb, &bar[pst], pol);
+        else
+            bulk_load_nohint(ring + (size_t)pst * rowb, px, rowb, &bar[pst]);
         px += row_step;
         if (++pst == S) pst = 0;
         ++issued;

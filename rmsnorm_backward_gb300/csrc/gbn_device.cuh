@@ -168,6 +168,14 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// 1-D bulk copy without an L2 cache hint
+__device__ __forceinline__ void bulk_load_nohint(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
 // L2 policy for data read exactly once (evict first)
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
@@ -321,6 +329,51 @@ __device__ __forceinline__ float block_sum(float v, float *sm) {
     for (int w = 1; w < nw; ++w) s += sm[w];
     __syncthreads();
     return s;
+}
+
+}  // namespace gbn
+
+namespace gbn {
+
+// ---------------------------------------------------------------------------
+// dgamma / dbeta column sums of the [G][ldp] partial rows, in one fixed order
+// ---------------------------------------------------------------------------
+constexpr int kColsumSlices = 16;
+
+// out[c] = sum over g < G of P[g*ldp + c], for c in [c0, c1), 32 columns a
+// pass: lane q of slice s (threads 32*s + q, s < 16) adds rows s, s+16, ...
+// in increasing order (eight loads issued together), then slice 0 adds the
+// 16 slice sums in slice order.  Every CTA shape that calls this gives the
+// same bits per column.  Needs at least 512 threads (the others only join
+// the barriers) and sm[16][33].  P is read through L2 (written by an
+// earlier grid).
+__device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int c0, int c1, float *out,
+                                             float (*sm)[33]) {
+    const int q = threadIdx.x & 31, slice = threadIdx.x >> 5;
+    for (int cb = c0; cb < c1; cb += 32) {
+        const int c = cb + q;
+        float a = 0.f;
+        if (slice < kColsumSlices && c < c1) {
+            for (int g0 = slice; g0 < G; g0 += kColsumSlices * 8) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int g = g0 + u * kColsumSlices;
+                    v[u] = g < G ? __ldcg(P + (size_t)g * ldp + c) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) a += v[u];
+            }
+        }
+        if (slice < kColsumSlices) sm[slice][q] = a;
+        __syncthreads();
+        if (slice == 0 && c < c1) {
+            float t = sm[0][q];
+            for (int s2 = 1; s2 < kColsumSlices; ++s2) t += sm[s2][q];
+            out[c] = t;
+        }
+        __syncthreads();
+    }
 }
 
 }  // namespace gbn

@@ -31,6 +31,7 @@ struct FwdParams {
     int stages;     // staged: ring stages per row slot
     int stat_rows;  // unused by the forward (kept for a uniform layout)
     int *err;       // the device's error flag
+    int l2_hint;    // bulk loads carry an L2 evict-first hint
 };
 
 struct BwdParams {
@@ -49,6 +50,7 @@ struct BwdParams {
     int stages;
     int stat_rows;      // capacity, in rows, of the staged statistics
     int *err;           // the device's error flag
+    int l2_hint;        // bulk loads carry an L2 evict-first hint
 };
 
 // Shared-memory layout of the staged kernels, computed identically on the

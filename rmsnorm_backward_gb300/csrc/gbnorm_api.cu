@@ -52,7 +52,9 @@ bool valid_dtype(int dtype) { return dtype == GBN_F32 || dtype == GBN_F16 || dty
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Optional overrides for experiments: GBN_GRID forces G, GBN_WARPS_PER_ROW the
-// slot width, GBN_NO_FULL=1 the bounds-checked kernel variants.
+// slot width, GBN_NO_FULL=1 the bounds-checked kernel variants, GBN_L2_HINT=1
+// bulk loads with an L2
+// evict-first hint (measured ~2 us slower on the 16384 x 4096 backward).
 int env_int(const char *name) {
     const char *v = std::getenv(name);
     return v ? std::atoi(v) : 0;
@@ -89,23 +91,25 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     const int V = 16 / es;
     if (N % V != 0) return P;
     const int64_t nvec = N / V;
-    // Slot width W warps.  Backward: the smallest that keeps a thread within
-    // the elements it can hold in registers between the two passes (16 for
-    // LayerNorm, 32 for RMSNorm), else up to kMaxVecPerThread vectors.
-    // Forward: the smallest with up to kMaxVecPerThread vectors per thread.
-    // (More rows in flight per CTA measured faster than fewer elements per
-    // thread.)
-    const int hold_elems = ln ? 16 : 32;
-    const int hold_vecs = bwd && hold_elems / V < kMaxVecPerThread ? hold_elems / V : kMaxVecPerThread;
+    // Slot width W warps: the smallest W whose threads cover the row within
+    // a cap on the vectors a thread owns, trying the caps in order.
+    // Backward: 16 elements (xhat, dyhat held in registers), then for
+    // RMSNorm 32 (raw x and dyhat held), then kMaxVecPerThread vectors
+    // (re-read).  Forward: kMaxVecPerThread vectors (more rows in flight per
+    // CTA measured faster than fewer elements per thread).
+    int caps[3] = {kMaxVecPerThread, kMaxVecPerThread, kMaxVecPerThread};
+    if (bwd) {
+        caps[0] = 16 / V < kMaxVecPerThread ? 16 / V : kMaxVecPerThread;
+        caps[1] = !ln && 32 / V < kMaxVecPerThread ? 32 / V : kMaxVecPerThread;
+    }
     int W = 0;
     const int forced = env_int("GBN_WARPS_PER_ROW");
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16) {
         if ((int64_t)32 * forced * kMaxVecPerThread >= nvec) W = forced;
     }
-    for (int pass = 0; pass < 2 && !W; ++pass) {
-        const int cap = pass == 0 ? hold_vecs : kMaxVecPerThread;
+    for (int pass = 0; pass < 3 && !W; ++pass) {
         for (int w = 1; w <= kRingThreads / 32; w *= 2) {
-            if ((int64_t)32 * w * cap >= nvec) {
+            if ((int64_t)32 * w * caps[pass] >= nvec) {
                 W = w;
                 break;
             }
@@ -117,7 +121,7 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     // exact tiling drops the bounds checks, except in the x-holding backward
     // mode, where the unchecked variant measured slower (register spills)
     P.full = (int64_t)P.nv * P.tpr == nvec && env_int("GBN_NO_FULL") == 0 &&
-             !(bwd && bwd_hold_mode(ln, P.nv * V) == kHoldX);
+             !(bwd && bwd_hold_mode(ln, P.nv * V) == kHoldX && P.nv * V > 16);
     P.stat_rows = static_cast<int>((M + G - 1) / G);
     const int slots = kRingThreads / P.tpr;
     // as many stages as fit, at most 16 per slot
@@ -135,12 +139,14 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     return P;
 }
 
+// Workspace: from its first 256-byte boundary, the [G, ldp] partial rows
+// (twice for LayerNorm).
 size_t workspace_bytes(int64_t M, int64_t N, bool ln, const DevInfo &d) {
     const int G = grid_rows(M, d);
     return (size_t)G * partial_ld(N) * 4 * (ln ? 2 : 1) + 256;
 }
 
-float *workspace_base(void *ws) {
+float *workspace_partials(void *ws) {
     const uintptr_t p = (reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255);
     return reinterpret_cast<float *>(p);
 }
@@ -170,6 +176,7 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
     FwdParams p{};
     p.x = x; p.gamma = gamma; p.beta = beta; p.y = y; p.mean = mean; p.rstd = rstd; p.eps = eps;
     p.M = M; p.N = static_cast<int>(N); p.G = grid_rows(M, d); p.err = d.err;
+    p.l2_hint = env_int("GBN_L2_HINT") != 0;
     const bool aligned = aligned16(x) && aligned16(y) && aligned16(gamma) && (!ln || aligned16(beta));
     StagedPlan P;
     if (aligned) P = staged_plan(false, ln, dtype, M, N, p.G, d);
@@ -192,8 +199,9 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
     BwdParams p{};
     p.dy = dy; p.x = x; p.gamma = gamma; p.mean = mean; p.rstd = rstd; p.dx = dx;
-    p.part = workspace_base(workspace);
+    p.part = workspace_partials(workspace);
     p.M = M; p.N = static_cast<int>(N); p.ldp = partial_ld(N); p.G = grid_rows(M, d); p.err = d.err;
+    p.l2_hint = env_int("GBN_L2_HINT") != 0;
     const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma);
     StagedPlan P;
     if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
@@ -219,7 +227,7 @@ int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, 
     if ((st = device_info(&d)) != GBN_OK) return st;
     if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
     const int G = grid_rows(M, d);
-    return cuda_status(launch_colsum(workspace_base(const_cast<void *>(workspace)), G, partial_ld(N),
+    return cuda_status(launch_colsum(workspace_partials(const_cast<void *>(workspace)), G, partial_ld(N),
                                      static_cast<int>(N), dgamma, ln ? dbeta : nullptr, stream));
 }
 

@@ -14,11 +14,9 @@ namespace gbn {
 
 static __device__ int g_error_flag = 0;
 
-// dgamma[j] (blockIdx.y = 0) or dbeta[j] (blockIdx.y = 1) = sum over g of
-// part[g][j].  Thread (slice, q) sums rows g = slice, slice + 16, ... of
-// column 32*blockIdx.x + q in that order (its loads issued together), then
-// the 16 slice sums are added in slice order: a fixed order per column.
-constexpr int kColsumSlices = 16;
+// dgamma (blockIdx.y = 0) or dbeta (blockIdx.y = 1): CTA x sums columns
+// [32x, 32x + 32) of the partial rows with colsum_range, the same order the
+// fused reduce of the staged backward uses.
 __global__ void __launch_bounds__(32 * kColsumSlices) colsum_kernel(const float *__restrict__ part, int G, int ldp,
                                                                      int N, float *__restrict__ dgamma,
                                                                      float *__restrict__ dbeta) {
@@ -26,28 +24,8 @@ __global__ void __launch_bounds__(32 * kColsumSlices) colsum_kernel(const float 
     griddep_wait();  // the partial rows of the kernel before this one
     const float *P = part + (size_t)blockIdx.y * G * ldp;
     float *out = blockIdx.y ? dbeta : dgamma;
-    const int q = threadIdx.x & 31, slice = threadIdx.x >> 5;
-    const int c = blockIdx.x * 32 + q;
-    float a = 0.f;
-    if (c < N) {
-        for (int g0 = slice; g0 < G; g0 += kColsumSlices * 8) {
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int g = g0 + u * kColsumSlices;
-                v[u] = g < G ? __ldcg(P + (size_t)g * ldp + c) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) a += v[u];
-        }
-    }
-    sm[slice][q] = a;
-    __syncthreads();
-    if (slice == 0 && c < N) {
-        float t = sm[0][q];
-        for (int s2 = 1; s2 < kColsumSlices; ++s2) t += sm[s2][q];
-        out[c] = t;
-    }
+    const int c0 = blockIdx.x * 32;
+    colsum_range(P, G, ldp, c0, min(N, c0 + 32), out, sm);
 }
 
 // ---------------------------------------------------------------------------

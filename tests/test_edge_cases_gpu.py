@@ -192,3 +192,17 @@ def test_argument_errors_are_reported():
     with pytest.raises(ValueError):
         gbn.rms_fwd(x.cpu(), g, 1e-6)
     assert gbn.device_error() == 0
+
+
+def test_reused_workspace_keeps_working():
+    """Many backward calls on one workspace give the first call's bits."""
+    w = wl.WORKLOADS["rms_bf16_16384x4096"].with_shape(1000, 4096)
+    d = {k: v.cuda() for k, v in wl.make_inputs(w).items()}
+    ws = torch.empty(gbn.bwd_workspace_bytes(w.M, w.N, torch.bfloat16, False), dtype=torch.uint8, device="cuda")
+    _, rstd = gbn.rms_fwd(d["x"], d["gamma"], w.eps)
+    dx0, dg0 = gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd, workspace=ws)
+    for _ in range(20):
+        dx, dg = gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dg, dg0) and torch.equal(dx, dx0)
+    assert gbn.device_error() == 0
