@@ -339,6 +339,7 @@ namespace gbn {
 // dgamma / dbeta column sums of the [G][ldp] partial rows, in one fixed order
 // ---------------------------------------------------------------------------
 constexpr int kColsumSlices = 16;
+constexpr int kColsumBatch = 8;  // loads a thread issues together (16 measured no faster)
 
 // out[c] = sum over g < G of P[g*ldp + c], for c in [c0, c1), 32 columns a
 // pass: lane q of slice s (threads 32*s + q, s < 16) adds rows s, s+16, ...
@@ -354,15 +355,15 @@ __device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int
         const int c = cb + q;
         float a = 0.f;
         if (slice < kColsumSlices && c < c1) {
-            for (int g0 = slice; g0 < G; g0 += kColsumSlices * 8) {
-                float v[8];
+            for (int g0 = slice; g0 < G; g0 += kColsumSlices * kColsumBatch) {
+                float v[kColsumBatch];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kColsumBatch; ++u) {
                     const int g = g0 + u * kColsumSlices;
                     v[u] = g < G ? __ldcg(P + (size_t)g * ldp + c) : 0.f;
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) a += v[u];
+                for (int u = 0; u < kColsumBatch; ++u) a += v[u];
             }
         }
         if (slice < kColsumSlices) sm[slice][q] = a;
