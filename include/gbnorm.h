@@ -136,6 +136,52 @@ int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
             void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Options of the extended calls below.  A NULL options pointer, or a
+ * zero-initialised struct, means: contiguous rows, outputs overwritten,
+ * dgamma / dbeta in float32 -- exactly the plain calls above.
+ *   ld_x, ld_dy, ld_out: row strides in elements of x, dy and the row output
+ *     (y in the forward, dx in the backward); 0 means N, else >= N.  Rows
+ *     stay contiguous within themselves ("Norm backward in Triton",
+ *     "The dx kernel": the stride_row argument).  The bulk-copy staged
+ *     kernels need every stride times the element size to be a multiple of
+ *     16 bytes; other strides take the plain-load kernels.
+ *   accumulate (backward): 1 adds this call's sums to what dgamma / dbeta
+ *     hold ("Matmul backward in Triton", the grad buffer is accumulated
+ *     into, never overwritten); the previous value is added after the
+ *     fixed-order sum, so the result stays deterministic.  With M = 0 the
+ *     buffers are left as they are.
+ *   grad_dtype (backward): storage type of dgamma / dbeta: GBN_F32 (the
+ *     default) or the dtype of the call (the parameters' own type, the cast
+ *     the pages' reduce kernels apply at the end), rounded to nearest even.
+ */
+typedef struct {
+    int64_t ld_x;
+    int64_t ld_dy;
+    int64_t ld_out;
+    int accumulate;
+    int grad_dtype;
+} gbn_options;
+
+/* The four operations with gbn_options; dgamma / dbeta are `void *` of type
+ * opt->grad_dtype.  Everything else as in the plain calls. */
+int ln_fwd_ex(const void *x, const void *gamma, const void *beta, void *y,
+              float *mean, float *rstd, float eps, int64_t M, int64_t N,
+              int dtype, const gbn_options *opt, cudaStream_t stream);
+int rms_fwd_ex(const void *x, const void *gamma, void *y, float *rstd,
+               float eps, int64_t M, int64_t N, int dtype,
+               const gbn_options *opt, cudaStream_t stream);
+int ln_bwd_ex(const void *dy, const void *x, const void *gamma,
+              const float *mean, const float *rstd, void *dx, void *dgamma,
+              void *dbeta, float eps, int64_t M, int64_t N, int dtype,
+              void *workspace, size_t workspace_bytes, const gbn_options *opt,
+              cudaStream_t stream);
+int rms_bwd_ex(const void *dy, const void *x, const void *gamma,
+               const float *rstd, void *dx, void *dgamma, float eps,
+               int64_t M, int64_t N, int dtype, void *workspace,
+               size_t workspace_bytes, const gbn_options *opt,
+               cudaStream_t stream);
+
+/*
  * rms_bwd_noalloc: rms_bwd for callers that cannot allocate device memory.
  * The pages have no counterpart to this call; it is a packaging of rms_bwd.
  *

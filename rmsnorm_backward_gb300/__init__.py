@@ -23,7 +23,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = [
-    "GbnError", "lib", "library_path", "ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd",
+    "GbnError", "GbnOptions", "lib", "library_path", "ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd",
     "ln_bwd_rows", "rms_bwd_rows", "bwd_reduce", "bwd_workspace_bytes", "bwd_plan",
     "device_error", "status_string", "DTYPE_CODES",
 ]
@@ -44,6 +44,13 @@ _f = ctypes.c_float
 _sz = ctypes.c_size_t
 
 
+class GbnOptions(ctypes.Structure):
+    """gbn_options of include/gbnorm.h."""
+
+    _fields_ = [("ld_x", ctypes.c_int64), ("ld_dy", ctypes.c_int64), ("ld_out", ctypes.c_int64),
+                ("accumulate", ctypes.c_int), ("grad_dtype", ctypes.c_int)]
+
+
 class GbnError(RuntimeError):
     """A libgbnorm call returned a non-zero gbn_status."""
 
@@ -62,11 +69,17 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ln_bwd_rows.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
     L.rms_bwd_rows.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
     L.gbn_bwd_reduce.argtypes = [_vp, _sz, _i64, _i64, _int, _int, _vp, _vp, _vp]
+    opt = ctypes.POINTER(GbnOptions)
+    L.ln_fwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, opt, _vp]
+    L.rms_fwd_ex.argtypes = [_vp, _vp, _vp, _vp, _f, _i64, _i64, _int, opt, _vp]
+    L.ln_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, opt, _vp]
+    L.rms_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, opt, _vp]
     L.gbn_bwd_plan.argtypes = [_i64, _i64, _int, _int, ctypes.POINTER(_int), ctypes.POINTER(_int)]
     L.gbn_device_error.argtypes = [_int]
     L.gbn_status_string.argtypes = [_int]
     L.gbn_status_string.restype = ctypes.c_char_p
-    for name in ("ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd", "ln_bwd_rows", "rms_bwd_rows",
+    for name in ("ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd", "ln_fwd_ex", "rms_fwd_ex", "ln_bwd_ex", "rms_bwd_ex",
+                 "ln_bwd_rows", "rms_bwd_rows",
                  "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error"):
         getattr(L, name).restype = _int
     return L
@@ -96,14 +109,30 @@ def _check(fn: str, status: int) -> None:
 
 
 def _rows(t: torch.Tensor, name: str) -> Tuple[int, int]:
+    M, N, _ = _rows_ld(t, name)
+    return M, N
+
+
+def _rows_ld(t: torch.Tensor, name: str) -> Tuple[int, int, int]:
+    """(M, N, row stride): a contiguous tensor with N = last dimension, or a
+    2-D view whose rows are contiguous (stride(1) == 1, stride(0) >= N)."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
     if t.dim() < 1:
         raise ValueError(f"{name} must have a feature dimension")
     N = t.shape[-1]
-    return (t.numel() // N if N else 0), N
+    if t.is_contiguous():
+        return (t.numel() // N if N else 0), N, N
+    if t.dim() == 2 and t.stride(1) == 1 and t.stride(0) >= N:
+        return t.shape[0], N, t.stride(0)
+    raise ValueError(f"{name} must be contiguous, or a 2-D view with contiguous rows")
+
+
+def _same_rows(t: torch.Tensor, ref: torch.Tensor, name: str) -> int:
+    """Row stride of t, which must have ref's shape, dtype and device."""
+    if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+        raise ValueError(f"{name} must have x's shape, dtype and device")
+    return _rows_ld(t, name)[2]
 
 
 def _code(t: torch.Tensor) -> int:
@@ -151,53 +180,57 @@ def device_error(clear: bool = True, device=None) -> int:
         return int(lib().gbn_device_error(int(clear)))
 
 
+def _options(ld_x: int, ld_dy: int, ld_out: int, accumulate: bool = False, grad_dtype=torch.float32):
+    return GbnOptions(ld_x, ld_dy, ld_out, int(bool(accumulate)), DTYPE_CODES[grad_dtype])
+
+
 def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float, *,
            y: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
            rstd: Optional[torch.Tensor] = None, stream=None):
-    """LayerNorm forward over the last dimension. Returns (y, mean, rstd)."""
-    M, N = _rows(x, "x")
-    y = torch.empty_like(x) if y is None else y
+    """LayerNorm forward over the last dimension. Returns (y, mean, rstd).
+
+    x may be a 2-D view with contiguous rows (any row stride); y likewise."""
+    M, N, ld_x = _rows_ld(x, "x")
+    y = torch.empty(x.shape, dtype=x.dtype, device=x.device) if y is None else y
     mean = torch.empty(M, dtype=torch.float32, device=x.device) if mean is None else mean
     rstd = torch.empty(M, dtype=torch.float32, device=x.device) if rstd is None else rstd
     for name, t in (("gamma", gamma), ("beta", beta)):
         _vec(t, name, N, x.dtype, x.device)
     _vec(mean, "mean", M, torch.float32, x.device)
     _vec(rstd, "rstd", M, torch.float32, x.device)
-    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous():
-        raise ValueError("y must be contiguous, with x's shape and dtype")
+    ld_y = _same_rows(y, x, "y")
+    opt = _options(ld_x, N, ld_y)
     with torch.cuda.device(x.device):
-        _check("ln_fwd", lib().ln_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
-                                      float(eps), M, N, _code(x), _stream(x.device, stream)))
+        _check("ln_fwd", lib().ln_fwd_ex(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
+                                         float(eps), M, N, _code(x), ctypes.byref(opt), _stream(x.device, stream)))
     return y, mean, rstd
 
 
 def rms_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, *, y: Optional[torch.Tensor] = None,
             rstd: Optional[torch.Tensor] = None, stream=None):
     """RMSNorm forward over the last dimension. Returns (y, rstd)."""
-    M, N = _rows(x, "x")
-    y = torch.empty_like(x) if y is None else y
+    M, N, ld_x = _rows_ld(x, "x")
+    y = torch.empty(x.shape, dtype=x.dtype, device=x.device) if y is None else y
     rstd = torch.empty(M, dtype=torch.float32, device=x.device) if rstd is None else rstd
     _vec(gamma, "gamma", N, x.dtype, x.device)
     _vec(rstd, "rstd", M, torch.float32, x.device)
-    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous():
-        raise ValueError("y must be contiguous, with x's shape and dtype")
+    ld_y = _same_rows(y, x, "y")
+    opt = _options(ld_x, N, ld_y)
     with torch.cuda.device(x.device):
-        _check("rms_fwd", lib().rms_fwd(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), float(eps), M, N,
-                                        _code(x), _stream(x.device, stream)))
+        _check("rms_fwd", lib().rms_fwd_ex(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), float(eps), M, N, _code(x),
+                                           ctypes.byref(opt), _stream(x.device, stream)))
     return y, rstd
 
 
-def _bwd_args(dy, x, gamma, stats, dx, ln):
-    M, N = _rows(x, "x")
-    if dy.shape != x.shape or dy.dtype != x.dtype or not dy.is_contiguous() or dy.device != x.device:
-        raise ValueError("dy must be contiguous, with x's shape, dtype and device")
+def _bwd_args(dy, x, gamma, stats, dx):
+    M, N, ld_x = _rows_ld(x, "x")
+    ld_dy = _same_rows(dy, x, "dy")
     _vec(gamma, "gamma", N, x.dtype, x.device)
     for name, t in stats:
         _vec(t, name, M, torch.float32, x.device)
-    dx = torch.empty_like(x) if dx is None else dx
-    if dx.shape != x.shape or dx.dtype != x.dtype or not dx.is_contiguous():
-        raise ValueError("dx must be contiguous, with x's shape and dtype")
-    return M, N, dx
+    dx = torch.empty(x.shape, dtype=x.dtype, device=x.device) if dx is None else dx
+    ld_dx = _same_rows(dx, x, "dx")
+    return M, N, dx, (ld_x, ld_dy, ld_dx)
 
 
 def _workspace(workspace, M, N, x, ln):
@@ -209,38 +242,56 @@ def _workspace(workspace, M, N, x, ln):
     return workspace, workspace.numel() * workspace.element_size()
 
 
+def _grads(t, name, N, grad_dtype, device, accumulate):
+    if t is None:
+        return (torch.zeros if accumulate else torch.empty)(N, dtype=grad_dtype, device=device)
+    _vec(t, name, N, grad_dtype, device)
+    return t
+
+
 def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor, *,
-           dx=None, dgamma=None, dbeta=None, workspace=None, stream=None):
-    """LayerNorm backward from the saved mean / rstd. Returns (dx, dgamma, dbeta); grads are fp32."""
-    M, N, dx = _bwd_args(dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx, True)
-    dgamma = torch.empty(N, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
-    dbeta = torch.empty(N, dtype=torch.float32, device=x.device) if dbeta is None else dbeta
-    _vec(dgamma, "dgamma", N, torch.float32, x.device)
-    _vec(dbeta, "dbeta", N, torch.float32, x.device)
+           dx=None, dgamma=None, dbeta=None, workspace=None, accumulate: bool = False, grad_dtype=torch.float32,
+           stream=None):
+    """LayerNorm backward from the saved mean / rstd. Returns (dx, dgamma, dbeta).
+
+    dgamma / dbeta are float32 unless grad_dtype is x's dtype; with
+    accumulate=True this call's sums are added to what they hold.  x, dy and
+    dx may be 2-D views with contiguous rows."""
+    if grad_dtype not in (torch.float32, x.dtype):
+        raise ValueError("grad_dtype must be float32 or x's dtype")
+    M, N, dx, (ld_x, ld_dy, ld_dx) = _bwd_args(dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx)
+    dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
+    dbeta = _grads(dbeta, "dbeta", N, grad_dtype, x.device, accumulate)
     workspace, wsb = _workspace(workspace, M, N, x, True)
+    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype)
     with torch.cuda.device(x.device):
-        _check("ln_bwd", lib().ln_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
-                                      _ptr(dgamma), _ptr(dbeta), 0.0, M, N, _code(x), _ptr(workspace), wsb,
-                                      _stream(x.device, stream)))
+        _check("ln_bwd", lib().ln_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                         _ptr(dgamma), _ptr(dbeta), 0.0, M, N, _code(x), _ptr(workspace), wsb,
+                                         ctypes.byref(opt), _stream(x.device, stream)))
     return dx, dgamma, dbeta
 
 
 def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: torch.Tensor, *,
-            dx=None, dgamma=None, workspace=None, stream=None):
-    """RMSNorm backward from the saved rstd. Returns (dx, dgamma); dgamma is fp32."""
-    M, N, dx = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx, False)
-    dgamma = torch.empty(N, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
-    _vec(dgamma, "dgamma", N, torch.float32, x.device)
+            dx=None, dgamma=None, workspace=None, accumulate: bool = False, grad_dtype=torch.float32, stream=None):
+    """RMSNorm backward from the saved rstd. Returns (dx, dgamma); options as for ln_bwd."""
+    if grad_dtype not in (torch.float32, x.dtype):
+        raise ValueError("grad_dtype must be float32 or x's dtype")
+    M, N, dx, (ld_x, ld_dy, ld_dx) = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx)
+    dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
     workspace, wsb = _workspace(workspace, M, N, x, False)
+    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype)
     with torch.cuda.device(x.device):
-        _check("rms_bwd", lib().rms_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
-                                        0.0, M, N, _code(x), _ptr(workspace), wsb, _stream(x.device, stream)))
+        _check("rms_bwd", lib().rms_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
+                                           0.0, M, N, _code(x), _ptr(workspace), wsb, ctypes.byref(opt),
+                                           _stream(x.device, stream)))
     return dx, dgamma
 
 
 def ln_bwd_rows(dy, x, gamma, mean, rstd, *, dx=None, workspace, stream=None):
     """Phase 1 of ln_bwd: dx and the per-CTA partial rows in ``workspace``. Returns dx."""
-    M, N, dx = _bwd_args(dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx, True)
+    M, N, dx, lds = _bwd_args(dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx)
+    if lds != (N, N, N):
+        raise ValueError("the backward phases take contiguous rows")
     workspace, wsb = _workspace(workspace, M, N, x, True)
     with torch.cuda.device(x.device):
         _check("ln_bwd_rows", lib().ln_bwd_rows(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd),
@@ -251,7 +302,9 @@ def ln_bwd_rows(dy, x, gamma, mean, rstd, *, dx=None, workspace, stream=None):
 
 def rms_bwd_rows(dy, x, gamma, rstd, *, dx=None, workspace, stream=None):
     """Phase 1 of rms_bwd: dx and the per-CTA partial rows in ``workspace``. Returns dx."""
-    M, N, dx = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx, False)
+    M, N, dx, lds = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx)
+    if lds != (N, N, N):
+        raise ValueError("the backward phases take contiguous rows")
     workspace, wsb = _workspace(workspace, M, N, x, False)
     with torch.cuda.device(x.device):
         _check("rms_bwd_rows", lib().rms_bwd_rows(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), M, N,

@@ -87,19 +87,19 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     __syncthreads();
 
     // producer (thread 0 of the slot): the slot's rows in order
-    const size_t row_step = (size_t)slots * N;
+    const size_t row_step = (size_t)slots * p.ld_dx;
     int issued = 0, pst = 0;
     auto issue = [&]() {
-        const size_t off = (size_t)(row0 + slot + (int64_t)issued * slots) * N;
+        const int64_t row = row0 + slot + (int64_t)issued * slots;
         unsigned char *dst = ring + (size_t)pst * stage_bytes;
         mbar_arrive_expect_tx(&bar[pst], stage_bytes);
         if (p.l2_hint) {
             const uint64_t pol = policy_evict_first();
-            bulk_load(dst, static_cast<const T *>(p.x) + off, rowb, &bar[pst], pol);
-            bulk_load(dst + rowb, static_cast<const T *>(p.dy) + off, rowb, &bar[pst], pol);
+            bulk_load(dst, static_cast<const T *>(p.x) + row * p.ld_x, rowb, &bar[pst], pol);
+            bulk_load(dst + rowb, static_cast<const T *>(p.dy) + row * p.ld_dy, rowb, &bar[pst], pol);
         } else {
-            bulk_load_nohint(dst, static_cast<const T *>(p.x) + off, rowb, &bar[pst]);
-            bulk_load_nohint(dst + rowb, static_cast<const T *>(p.dy) + off, rowb, &bar[pst]);
+            bulk_load_nohint(dst, static_cast<const T *>(p.x) + row * p.ld_x, rowb, &bar[pst]);
+            bulk_load_nohint(dst + rowb, static_cast<const T *>(p.dy) + row * p.ld_dy, rowb, &bar[pst]);
         }
         if (++pst == S) pst = 0;
         ++issued;
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     griddep_launch_dependents();
 
     const float inv_n = 1.0f / static_cast<float>(N);
-    T *dxrow = static_cast<T *>(p.dx) + (row0 + slot) * N + (size_t)ts * V;
+    T *dxrow = static_cast<T *>(p.dx) + (row0 + slot) * p.ld_dx + (size_t)ts * V;
     RingPos pos;
     int k = 0;
     for (; k < ns; ++k) {
@@ -333,8 +333,8 @@ __global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdPar
     const T *g = static_cast<const T *>(p.gamma);
     for (int i = 0; i < nrows; ++i) {
         const int64_t row = row0 + i;
-        const T *xr = static_cast<const T *>(p.x) + row * N;
-        const T *dyr = static_cast<const T *>(p.dy) + row * N;
+        const T *xr = static_cast<const T *>(p.x) + row * p.ld_x;
+        const T *dyr = static_cast<const T *>(p.dy) + row * p.ld_dy;
         const float rs = p.rstd[row];
         const float mu = LN ? p.mean[row] : 0.f;
         float s1 = 0.f, s2 = 0.f;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdPar
         }
         const float a = -rs * (block_sum(s2, sm) * inv_n);
         const float b = LN ? -rs * (block_sum(s1, sm) * inv_n) : 0.f;
-        T *dxr = static_cast<T *>(p.dx) + row * N;
+        T *dxr = static_cast<T *>(p.dx) + row * p.ld_dx;
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
             const float xhat = (Tr::load1(xr + j) - mu) * rs;
             const float dy = Tr::load1(dyr + j);

@@ -71,8 +71,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
     __syncthreads();
 
     const uint64_t pol = policy_evict_first();
-    const size_t row_step = (size_t)slots * N;
-    const T *px = static_cast<const T *>(p.x) + (row0 + slot) * N;
+    const size_t row_step = (size_t)slots * p.ld_y;
+    const size_t xrow_step = (size_t)slots * p.ld_x;
+    const T *px = static_cast<const T *>(p.x) + (row0 + slot) * p.ld_x;
     int issued = 0, pst = 0;
     auto issue = [&]() {
         mbar_arrive_expect_tx(&bar[pst], rowb);
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
             bulk_load(ring + (size_t)pst * rowb, px, rowb, &bar[pst], pol);
         else
             bulk_load_nohint(ring + (size_t)pst * rowb, px, rowb, &bar[pst]);
-        px += row_step;
+        px += xrow_step;
         if (++pst == S) pst = 0;
         ++issued;
     };
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
         }
     }
     const float inv_n = 1.0f / static_cast<float>(N);
-    T *yrow = static_cast<T *>(p.y) + (row0 + slot) * N + (size_t)ts * V;
+    T *yrow = static_cast<T *>(p.y) + (row0 + slot) * p.ld_y + (size_t)ts * V;
     int64_t row = row0 + slot;
     RingPos pos;
 
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kGenericThreads) fwd_plain_kernel(const FwdPar
     const int N = p.N;
     const float inv_n = 1.0f / static_cast<float>(N);
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
-        const T *xr = static_cast<const T *>(p.x) + row * N;
+        const T *xr = static_cast<const T *>(p.x) + row * p.ld_x;
         float mu = 0.f;
         if (LN) {
             float s = 0.f;
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kGenericThreads) fwd_plain_kernel(const FwdPar
             q = fmaf(d, d, q);
         }
         const float rs = 1.0f / sqrtf(block_sum(q, sm) * inv_n + p.eps);
-        T *yr = static_cast<T *>(p.y) + row * N;
+        T *yr = static_cast<T *>(p.y) + row * p.ld_y;
         const T *g = static_cast<const T *>(p.gamma);
         const T *b = static_cast<const T *>(p.beta);
         for (int j = threadIdx.x; j < N; j += blockDim.x) {

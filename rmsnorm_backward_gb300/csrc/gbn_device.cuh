@@ -341,14 +341,16 @@ namespace gbn {
 constexpr int kColsumSlices = 16;
 constexpr int kColsumBatch = 8;  // loads a thread issues together (16 measured no faster)
 
-// out[c] = sum over g < G of P[g*ldp + c], for c in [c0, c1), 32 columns a
+// sum over g < G of P[g*ldp + c], for c in [c0, c1), 32 columns a
 // pass: lane q of slice s (threads 32*s + q, s < 16) adds rows s, s+16, ...
 // in increasing order (eight loads issued together), then slice 0 adds the
 // 16 slice sums in slice order.  Every CTA shape that calls this gives the
 // same bits per column.  Needs at least 512 threads (the others only join
 // the barriers) and sm[16][33].  P is read through L2 (written by an
 // earlier grid).
-__device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int c0, int c1, float *out,
+// store(c, sum) writes the result of column c.
+template <typename Store>
+__device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int c0, int c1, Store store,
                                              float (*sm)[33]) {
     const int q = threadIdx.x & 31, slice = threadIdx.x >> 5;
     for (int cb = c0; cb < c1; cb += 32) {
@@ -371,7 +373,7 @@ __device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int
         if (slice == 0 && c < c1) {
             float t = sm[0][q];
             for (int s2 = 1; s2 < kColsumSlices; ++s2) t += sm[s2][q];
-            out[c] = t;
+            store(c, t);
         }
         __syncthreads();
     }

@@ -32,6 +32,8 @@ struct FwdParams {
     int stat_rows;  // unused by the forward (kept for a uniform layout)
     int *err;       // the device's error flag
     int l2_hint;    // bulk loads carry an L2 evict-first hint
+    int64_t ld_x;   // row strides, in elements, of x and y
+    int64_t ld_y;
 };
 
 struct BwdParams {
@@ -51,6 +53,9 @@ struct BwdParams {
     int stat_rows;      // capacity, in rows, of the staged statistics
     int *err;           // the device's error flag
     int l2_hint;        // bulk loads carry an L2 evict-first hint
+    int64_t ld_x;       // row strides, in elements, of x, dy and dx
+    int64_t ld_dy;
+    int64_t ld_dx;
 };
 
 // Shared-memory layout of the staged kernels, computed identically on the
@@ -108,8 +113,11 @@ cudaError_t launch_fwd_plain(int dtype, bool ln, const FwdParams &p, cudaStream_
 cudaError_t launch_bwd_staged(int dtype, bool ln, int nv, bool full, const BwdParams &p, size_t smem,
                               cudaStream_t s);
 cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_t s);
-cudaError_t launch_colsum(const float *part, int G, int ldp, int N, float *dgamma, float *dbeta,
-                          cudaStream_t s);
+// dgamma / dbeta from the partial rows; out_dtype is GBN_F32 or the storage
+// dtype of the parameters (rounded to nearest even); accumulate adds the
+// buffers' previous contents (widened) to the sums before the store
+cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
+                          bool accumulate, cudaStream_t s);
 
 // the current device's error flag: its device address, and a synchronising read
 cudaError_t error_flag_address(int **addr);

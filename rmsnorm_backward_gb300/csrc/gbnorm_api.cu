@@ -158,6 +158,28 @@ int check_shape(int64_t M, int64_t N, int dtype) {
     return GBN_OK;
 }
 
+// gbn_options resolved: strides in elements, accumulate, dgamma/dbeta dtype
+struct Opts {
+    int64_t ld_x = 0, ld_dy = 0, ld_out = 0;
+    bool accumulate = false;
+    int grad_dtype = GBN_F32;
+};
+
+int resolve_options(const gbn_options *o, int64_t N, int dtype, Opts *r) {
+    r->ld_x = o && o->ld_x ? o->ld_x : N;
+    r->ld_dy = o && o->ld_dy ? o->ld_dy : N;
+    r->ld_out = o && o->ld_out ? o->ld_out : N;
+    if (r->ld_x < N || r->ld_dy < N || r->ld_out < N) return GBN_EINVAL;
+    if (o && o->accumulate != 0 && o->accumulate != 1) return GBN_EINVAL;
+    r->accumulate = o && o->accumulate == 1;
+    r->grad_dtype = o ? o->grad_dtype : GBN_F32;
+    if (r->grad_dtype != GBN_F32 && r->grad_dtype != dtype) return GBN_EDTYPE;
+    return GBN_OK;
+}
+
+// rows starting on 16-byte boundaries, given a 16-byte aligned base
+bool stride16(int64_t ld, int dtype) { return (ld * elem_bytes(dtype)) % 16 == 0; }
+
 int cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return GBN_OK;
     cudaGetLastError();
@@ -165,7 +187,7 @@ int cuda_status(cudaError_t e) {
 }
 
 int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *y, float *mean, float *rstd,
-             float eps, int64_t M, int64_t N, int dtype, cudaStream_t stream) {
+             float eps, int64_t M, int64_t N, int dtype, const Opts &o, cudaStream_t stream) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (!(eps >= 0.f) || !isfinite(eps)) return GBN_EINVAL;
@@ -177,7 +199,9 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
     p.x = x; p.gamma = gamma; p.beta = beta; p.y = y; p.mean = mean; p.rstd = rstd; p.eps = eps;
     p.M = M; p.N = static_cast<int>(N); p.G = grid_rows(M, d); p.err = d.err;
     p.l2_hint = env_int("GBN_L2_HINT") != 0;
-    const bool aligned = aligned16(x) && aligned16(y) && aligned16(gamma) && (!ln || aligned16(beta));
+    p.ld_x = o.ld_x; p.ld_y = o.ld_out;
+    const bool aligned = aligned16(x) && aligned16(y) && aligned16(gamma) && (!ln || aligned16(beta)) &&
+                         stride16(o.ld_x, dtype) && stride16(o.ld_out, dtype);
     StagedPlan P;
     if (aligned) P = staged_plan(false, ln, dtype, M, N, p.G, d);
     if (P.ok) {
@@ -189,7 +213,7 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
 
 int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
                   void *dx, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes_given,
-                  cudaStream_t stream) {
+                  const Opts &o, cudaStream_t stream) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (M == 0) return GBN_OK;
@@ -202,7 +226,9 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     p.part = workspace_partials(workspace);
     p.M = M; p.N = static_cast<int>(N); p.ldp = partial_ld(N); p.G = grid_rows(M, d); p.err = d.err;
     p.l2_hint = env_int("GBN_L2_HINT") != 0;
-    const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma);
+    p.ld_x = o.ld_x; p.ld_dy = o.ld_dy; p.ld_dx = o.ld_out;
+    const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma) &&
+                         stride16(o.ld_x, dtype) && stride16(o.ld_dy, dtype) && stride16(o.ld_out, dtype);
     StagedPlan P;
     if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
     if (P.ok) {
@@ -213,13 +239,15 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
 }
 
 int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, int64_t N, int dtype, bool ln,
-                float *dgamma, float *dbeta, cudaStream_t stream) {
+                void *dgamma, void *dbeta, const Opts &o, cudaStream_t stream) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (!dgamma || (ln && !dbeta)) return GBN_EINVAL;
     if (M == 0) {
-        st = cuda_status(cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream));
-        if (st == GBN_OK && ln) st = cuda_status(cudaMemsetAsync(dbeta, 0, (size_t)N * 4, stream));
+        if (o.accumulate) return GBN_OK;  // nothing to add
+        const size_t bytes = (size_t)N * elem_bytes(o.grad_dtype);  // all-zero bits are 0.0 in every dtype
+        st = cuda_status(cudaMemsetAsync(dgamma, 0, bytes, stream));
+        if (st == GBN_OK && ln) st = cuda_status(cudaMemsetAsync(dbeta, 0, bytes, stream));
         return st;
     }
     if (!workspace) return GBN_EINVAL;
@@ -228,7 +256,8 @@ int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, 
     if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
     const int G = grid_rows(M, d);
     return cuda_status(launch_colsum(workspace_partials(const_cast<void *>(workspace)), G, partial_ld(N),
-                                     static_cast<int>(N), dgamma, ln ? dbeta : nullptr, stream));
+                                     static_cast<int>(N), dgamma, ln ? dbeta : nullptr, o.grad_dtype,
+                                     o.accumulate, stream));
 }
 
 }  // namespace
@@ -245,48 +274,93 @@ size_t gbn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta) {
     return workspace_bytes(M, N, has_beta != 0, d);
 }
 
+int ln_fwd_ex(const void *x, const void *gamma, const void *beta, void *y, float *mean, float *rstd, float eps,
+              int64_t M, int64_t N, int dtype, const gbn_options *opt, cudaStream_t stream) {
+    Opts o;
+    int st = check_shape(M, N, dtype);
+    if (st == GBN_OK) st = resolve_options(opt, N, dtype, &o);
+    if (st != GBN_OK) return st;
+    return fwd_impl(true, x, gamma, beta, y, mean, rstd, eps, M, N, dtype, o, stream);
+}
+
+int rms_fwd_ex(const void *x, const void *gamma, void *y, float *rstd, float eps, int64_t M, int64_t N, int dtype,
+               const gbn_options *opt, cudaStream_t stream) {
+    Opts o;
+    int st = check_shape(M, N, dtype);
+    if (st == GBN_OK) st = resolve_options(opt, N, dtype, &o);
+    if (st != GBN_OK) return st;
+    return fwd_impl(false, x, gamma, nullptr, y, nullptr, rstd, eps, M, N, dtype, o, stream);
+}
+
 int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean, float *rstd, float eps,
            int64_t M, int64_t N, int dtype, cudaStream_t stream) {
-    return fwd_impl(true, x, gamma, beta, y, mean, rstd, eps, M, N, dtype, stream);
+    return ln_fwd_ex(x, gamma, beta, y, mean, rstd, eps, M, N, dtype, nullptr, stream);
 }
 
 int rms_fwd(const void *x, const void *gamma, void *y, float *rstd, float eps, int64_t M, int64_t N, int dtype,
             cudaStream_t stream) {
-    return fwd_impl(false, x, gamma, nullptr, y, nullptr, rstd, eps, M, N, dtype, stream);
+    return rms_fwd_ex(x, gamma, y, rstd, eps, M, N, dtype, nullptr, stream);
 }
 
 int ln_bwd_rows(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
                 int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    return bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
+    Opts o;
+    o.ld_x = o.ld_dy = o.ld_out = N;
+    return bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream);
 }
 
 int rms_bwd_rows(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, int64_t M,
                  int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    return bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
+    Opts o;
+    o.ld_x = o.ld_dy = o.ld_out = N;
+    return bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, o,
+                         stream);
 }
 
 int gbn_bwd_reduce(const void *workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, int has_beta,
                    float *dgamma, float *dbeta, cudaStream_t stream) {
-    return reduce_impl(workspace, workspace_bytes, M, N, dtype, has_beta != 0, dgamma, dbeta, stream);
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, has_beta != 0, dgamma, dbeta, Opts(), stream);
+}
+
+int ln_bwd_ex(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
+              void *dgamma, void *dbeta, float eps, int64_t M, int64_t N, int dtype, void *workspace,
+              size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream) {
+    (void)eps;
+    Opts o;
+    int st = check_shape(M, N, dtype);
+    if (st == GBN_OK) st = resolve_options(opt, N, dtype, &o);
+    if (st != GBN_OK) return st;
+    if (M > 0 && (!dgamma || !dbeta)) return GBN_EINVAL;
+    st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream);
+    if (st != GBN_OK) return st;
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, o, stream);
+}
+
+int rms_bwd_ex(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, void *dgamma,
+               float eps, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes,
+               const gbn_options *opt, cudaStream_t stream) {
+    (void)eps;
+    Opts o;
+    int st = check_shape(M, N, dtype);
+    if (st == GBN_OK) st = resolve_options(opt, N, dtype, &o);
+    if (st != GBN_OK) return st;
+    if (M > 0 && !dgamma) return GBN_EINVAL;
+    st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream);
+    if (st != GBN_OK) return st;
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, o, stream);
 }
 
 int ln_bwd(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
            float *dgamma, float *dbeta, float eps, int64_t M, int64_t N, int dtype, void *workspace,
            size_t workspace_bytes, cudaStream_t stream) {
-    (void)eps;
-    if (M > 0 && (!dgamma || !dbeta)) return GBN_EINVAL;
-    int st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
-    if (st != GBN_OK) return st;
-    return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, stream);
+    return ln_bwd_ex(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, eps, M, N, dtype, workspace, workspace_bytes,
+                     nullptr, stream);
 }
 
 int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, float *dgamma, float eps,
             int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    (void)eps;
-    if (M > 0 && !dgamma) return GBN_EINVAL;
-    int st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, stream);
-    if (st != GBN_OK) return st;
-    return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, stream);
+    return rms_bwd_ex(dy, x, gamma, rstd, dx, dgamma, eps, M, N, dtype, workspace, workspace_bytes, nullptr,
+                      stream);
 }
 
 int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *staged) {

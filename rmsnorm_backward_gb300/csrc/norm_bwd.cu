@@ -7,6 +7,8 @@
 // section "The gradients"), summing the per-CTA partial rows in a fixed
 // order ("The hard half": a second, small kernel over the [GROUPS, d]
 // workspace), so the result does not depend on timing.
+#include <type_traits>
+
 #include "gbn_device.cuh"
 #include "gbn_launch.h"
 
@@ -15,17 +17,28 @@ namespace gbn {
 static __device__ int g_error_flag = 0;
 
 // dgamma (blockIdx.y = 0) or dbeta (blockIdx.y = 1): CTA x sums columns
-// [32x, 32x + 32) of the partial rows with colsum_range, the same order the
-// fused reduce of the staged backward uses.
+// [32x, 32x + 32) of the partial rows with colsum_range (one fixed order).
+template <typename OutT, bool ACC>
 __global__ void __launch_bounds__(32 * kColsumSlices) colsum_kernel(const float *__restrict__ part, int G, int ldp,
-                                                                     int N, float *__restrict__ dgamma,
-                                                                     float *__restrict__ dbeta) {
+                                                                     int N, OutT *__restrict__ dgamma,
+                                                                     OutT *__restrict__ dbeta) {
     __shared__ float sm[kColsumSlices][33];
     griddep_wait();  // the partial rows of the kernel before this one
     const float *P = part + (size_t)blockIdx.y * G * ldp;
-    float *out = blockIdx.y ? dbeta : dgamma;
+    OutT *out = blockIdx.y ? dbeta : dgamma;
     const int c0 = blockIdx.x * 32;
-    colsum_range(P, G, ldp, c0, min(N, c0 + 32), out, sm);
+    // accumulate: the buffer's previous value is added after the fixed-order
+    // sum; 16-bit outputs are rounded to nearest even
+    colsum_range(
+        P, G, ldp, c0, min(N, c0 + 32),
+        [&](int c, float t) {
+            if constexpr (std::is_same<OutT, float>::value) {
+                out[c] = ACC ? out[c] + t : t;
+            } else {
+                Traits<OutT>::store1(out + c, ACC ? Traits<OutT>::load1(out + c) + t : t);
+            }
+        },
+        sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -82,7 +95,8 @@ cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_colsum(const float *part, int G, int ldp, int N, float *dgamma, float *dbeta, cudaStream_t s) {
+template <typename OutT, bool ACC>
+cudaError_t launch_colsum_t(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + 31) / 32, dbeta ? 2 : 1);
     cfg.blockDim = dim3(32 * kColsumSlices);
@@ -93,7 +107,25 @@ cudaError_t launch_colsum(const float *part, int G, int ldp, int N, float *dgamm
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, colsum_kernel, part, G, ldp, N, dgamma, dbeta);
+    return cudaLaunchKernelEx(&cfg, colsum_kernel<OutT, ACC>, part, G, ldp, N, static_cast<OutT *>(dgamma),
+                              static_cast<OutT *>(dbeta));
+}
+
+template <typename OutT>
+cudaError_t launch_colsum_acc(const float *part, int G, int ldp, int N, void *dg, void *db, bool acc,
+                              cudaStream_t s) {
+    return acc ? launch_colsum_t<OutT, true>(part, G, ldp, N, dg, db, s)
+               : launch_colsum_t<OutT, false>(part, G, ldp, N, dg, db, s);
+}
+
+cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
+                          bool accumulate, cudaStream_t s) {
+    switch (out_dtype) {
+        case 0: return launch_colsum_acc<float>(part, G, ldp, N, dgamma, dbeta, accumulate, s);
+        case 1: return launch_colsum_acc<__half>(part, G, ldp, N, dgamma, dbeta, accumulate, s);
+        case 2: return launch_colsum_acc<__nv_bfloat16>(part, G, ldp, N, dgamma, dbeta, accumulate, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t error_flag_address(int **addr) {
