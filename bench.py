@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--stats", choices=["saved", "recompute"], default="saved",
+                    help="recompute: the backward gets no saved statistics and forms them from x")
     return ap.parse_args(argv)
 
 
@@ -189,7 +191,7 @@ class ClockSampler:
 class Problem:
     """Device buffers and the three launches of one step for a workload."""
 
-    def __init__(self, w: wl.Workload, device, stream):
+    def __init__(self, w: wl.Workload, device, stream, recompute: bool = False):
         import rmsnorm_backward_gb300 as gbn
 
         self.gbn = gbn
@@ -219,23 +221,33 @@ class Problem:
         code = gbn.DTYPE_CODES[tdt]
         M, N, P = w.M, w.N, (lambda t: None if t is None else t.data_ptr())
         wsb = self.ws.numel()
+        self.recompute = recompute
+        # the backward's statistics: the forward's, or none (formed from x)
+        bmean = None if recompute else self.mean
+        brstd = None if recompute else self.rstd
+        beps = w.eps if recompute else 0.0
         if w.has_beta:
             self._fwd = (L.ln_fwd, (P(self.x), P(self.gamma), P(self.beta), P(self.y), P(self.mean),
                                     P(self.rstd), w.eps, M, N, code, sp))
             self._rows = (L.ln_bwd_rows, (P(self.dy), P(self.x), P(self.gamma), P(self.mean), P(self.rstd),
                                           P(self.dx), M, N, code, P(self.ws), wsb, sp))
+            self._rows_recompute = (L.ln_bwd_ex, (P(self.dy), P(self.x), P(self.gamma), None, None, P(self.dx),
+                                                  P(self.dgamma), P(self.dbeta), w.eps, M, N, code, P(self.ws), wsb,
+                                                  None, sp))
         else:
             self._fwd = (L.rms_fwd, (P(self.x), P(self.gamma), P(self.y), P(self.rstd), w.eps, M, N, code, sp))
             self._rows = (L.rms_bwd_rows, (P(self.dy), P(self.x), P(self.gamma), P(self.rstd), P(self.dx), M, N,
                                            code, P(self.ws), wsb, sp))
+            self._rows_recompute = (L.rms_bwd_ex, (P(self.dy), P(self.x), P(self.gamma), None, P(self.dx),
+                                                   P(self.dgamma), w.eps, M, N, code, P(self.ws), wsb, None, sp))
         self._red = (L.gbn_bwd_reduce, (P(self.ws), wsb, M, N, code, int(w.has_beta), P(self.dgamma),
                                         P(self.dbeta), sp))
         if w.has_beta:
-            self._bwd = (L.ln_bwd, (P(self.dy), P(self.x), P(self.gamma), P(self.mean), P(self.rstd), P(self.dx),
-                                    P(self.dgamma), P(self.dbeta), 0.0, M, N, code, P(self.ws), wsb, sp))
+            self._bwd = (L.ln_bwd, (P(self.dy), P(self.x), P(self.gamma), P(bmean), P(brstd), P(self.dx),
+                                    P(self.dgamma), P(self.dbeta), beps, M, N, code, P(self.ws), wsb, sp))
         else:
-            self._bwd = (L.rms_bwd, (P(self.dy), P(self.x), P(self.gamma), P(self.rstd), P(self.dx),
-                                     P(self.dgamma), 0.0, M, N, code, P(self.ws), wsb, sp))
+            self._bwd = (L.rms_bwd, (P(self.dy), P(self.x), P(self.gamma), P(brstd), P(self.dx),
+                                     P(self.dgamma), beps, M, N, code, P(self.ws), wsb, sp))
 
     @staticmethod
     def _call(fn_args):
@@ -247,10 +259,13 @@ class Problem:
         self._call(self._fwd)
 
     def bwd_rows(self):
-        self._call(self._rows)
+        # the save-nothing backward has no separate rows phase: time the
+        # whole call (rows kernel + reduce) there
+        self._call(self._rows_recompute if self.recompute else self._rows)
 
     def bwd_reduce(self):
-        self._call(self._red)
+        if not self.recompute:
+            self._call(self._red)
 
     def bwd_fused(self):
         self._call(self._bwd)
@@ -418,7 +433,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device)
-    prob = Problem(w, device, stream)
+    prob = Problem(w, device, stream, recompute=args.stats == "recompute")
     flush = L2Flush(device)
     import rmsnorm_backward_gb300 as gbn
 
@@ -435,6 +450,8 @@ def run_ours(args):
     fwd_s = dist_max(float(fwd.sum()) / 1e3, world, device)
     K = args.steps
     bwd_bytes = wl.bwd_min_bytes(w.op, w.dtype, w.M, w.N)
+    if args.stats == "recompute":  # no statistics are read
+        bwd_bytes -= 4 * w.M * (2 if w.has_beta else 1)
     fwd_bytes = wl.fwd_min_bytes(w.op, w.dtype, w.M, w.N)
     value = world * K * bwd_bytes / bwd_s / 1e9
     peak, peak_src = measured_hbm_peak()
@@ -466,7 +483,7 @@ def run_ours(args):
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "l2": ("flushed before the forward and before the backward of every step: a 256 MiB write, "
                        "then a 256 MiB read of another buffer so no dirty lines carry into the timed kernel"),
-                "G": G, "staged_kernel": staged,
+                "G": G, "staged_kernel": staged, "stats": args.stats,
                 "step": "forward (y, stats) then backward (dx + partial rows, then column reduce)",
                 "timed": ("value = backward minimum bytes / device time of the public backward call (rows kernel "
                           "+ column reduce, CUDA events around the call); roofline = rows kernel alone, own loop"),
@@ -484,7 +501,8 @@ def run_ours(args):
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": "bwd_staged_kernel (dx + per-CTA partial rows)",
+                "kernel": ("bwd_staged_kernel (dx + per-CTA partial rows)" if args.stats == "saved" else
+                           "whole save-nothing backward call (rows kernel + column reduce)"),
                 "algorithmic_bytes_per_launch": rows_bytes, "peak_source": peak_src,
             },
             "e2e": {"value": round(world * bwd_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",

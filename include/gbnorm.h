@@ -113,8 +113,11 @@ int rms_fwd(const void *x, const void *gamma, void *y, float *rstd, float eps,
  * dbeta lines; the dx kernel recomputes xhat from the saved statistics).
  *   dy, x [M,N] dtype (in); gamma [N] dtype (in); mean, rstd [M] f32 (in,
  *   as written by ln_fwd); dx [M,N] dtype (out); dgamma, dbeta [N] f32 (out).
- *   eps is not used (rstd already holds it); it is accepted so that the four
- *   calls share one parameter list.
+ *   eps is used only when mean and rstd are both NULL: then nothing was
+ *   saved and the backward forms each row's mean and rstd from x itself,
+ *   as ln_fwd does ("Norm & activation backward", "Half one": the
+ *   save-nothing option of the save-vs-recompute table); x is read once
+ *   either way.  Passing only one of mean / rstd is GBN_EINVAL.
  *   workspace: device scratch of at least gbn_bwd_workspace_bytes(M, N,
  *   dtype, 1) bytes, owned by the caller; its contents on entry do not
  *   matter and on return are the per-CTA partials.  It must not be used by
@@ -128,8 +131,9 @@ int ln_bwd(const void *dy, const void *x, const void *gamma, const float *mean,
 
 /*
  * RMSNorm backward: LayerNorm's without the mean and without the mean(dyhat)
- * term, and without dbeta.  Arguments as for ln_bwd; the workspace size is
- * gbn_bwd_workspace_bytes(M, N, dtype, 0).
+ * term, and without dbeta.  Arguments as for ln_bwd (rstd NULL: recomputed
+ * from x with eps); the workspace size is gbn_bwd_workspace_bytes(M, N,
+ * dtype, 0).
  */
 int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
             void *dx, float *dgamma, float eps, int64_t M, int64_t N, int dtype,

@@ -249,16 +249,29 @@ def _grads(t, name, N, grad_dtype, device, accumulate):
     return t
 
 
-def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor, *,
-           dx=None, dgamma=None, dbeta=None, workspace=None, accumulate: bool = False, grad_dtype=torch.float32,
-           stream=None):
+def _recompute_eps(stats, eps):
+    """eps for the save-nothing backward (all statistics None), else 0."""
+    if all(t is None for t in stats):
+        if eps is None:
+            raise ValueError("without saved statistics the backward needs eps")
+        return float(eps)
+    if any(t is None for t in stats):
+        raise ValueError("pass all saved statistics or none")
+    return 0.0
+
+
+def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: Optional[torch.Tensor],
+           rstd: Optional[torch.Tensor], *, dx=None, dgamma=None, dbeta=None, workspace=None,
+           accumulate: bool = False, grad_dtype=torch.float32, eps: Optional[float] = None, stream=None):
     """LayerNorm backward from the saved mean / rstd. Returns (dx, dgamma, dbeta).
 
-    dgamma / dbeta are float32 unless grad_dtype is x's dtype; with
-    accumulate=True this call's sums are added to what they hold.  x, dy and
-    dx may be 2-D views with contiguous rows."""
+    With mean = rstd = None nothing was saved: the statistics are formed from
+    x with ``eps``.  dgamma / dbeta are float32 unless grad_dtype is x's
+    dtype; with accumulate=True this call's sums are added to what they
+    hold.  x, dy and dx may be 2-D views with contiguous rows."""
     if grad_dtype not in (torch.float32, x.dtype):
         raise ValueError("grad_dtype must be float32 or x's dtype")
+    eps_arg = _recompute_eps((mean, rstd), eps)
     M, N, dx, (ld_x, ld_dy, ld_dx) = _bwd_args(dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx)
     dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
     dbeta = _grads(dbeta, "dbeta", N, grad_dtype, x.device, accumulate)
@@ -266,23 +279,26 @@ def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.T
     opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype)
     with torch.cuda.device(x.device):
         _check("ln_bwd", lib().ln_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
-                                         _ptr(dgamma), _ptr(dbeta), 0.0, M, N, _code(x), _ptr(workspace), wsb,
+                                         _ptr(dgamma), _ptr(dbeta), eps_arg, M, N, _code(x), _ptr(workspace), wsb,
                                          ctypes.byref(opt), _stream(x.device, stream)))
     return dx, dgamma, dbeta
 
 
-def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: torch.Tensor, *,
-            dx=None, dgamma=None, workspace=None, accumulate: bool = False, grad_dtype=torch.float32, stream=None):
-    """RMSNorm backward from the saved rstd. Returns (dx, dgamma); options as for ln_bwd."""
+def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: Optional[torch.Tensor], *,
+            dx=None, dgamma=None, workspace=None, accumulate: bool = False, grad_dtype=torch.float32,
+            eps: Optional[float] = None, stream=None):
+    """RMSNorm backward from the saved rstd (None: recomputed from x with eps).
+    Returns (dx, dgamma); options as for ln_bwd."""
     if grad_dtype not in (torch.float32, x.dtype):
         raise ValueError("grad_dtype must be float32 or x's dtype")
+    eps_arg = _recompute_eps((rstd,), eps)
     M, N, dx, (ld_x, ld_dy, ld_dx) = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx)
     dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
     workspace, wsb = _workspace(workspace, M, N, x, False)
     opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype)
     with torch.cuda.device(x.device):
         _check("rms_bwd", lib().rms_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
-                                           0.0, M, N, _code(x), _ptr(workspace), wsb, ctypes.byref(opt),
+                                           eps_arg, M, N, _code(x), _ptr(workspace), wsb, ctypes.byref(opt),
                                            _stream(x.device, stream)))
     return dx, dgamma
 

@@ -39,7 +39,7 @@
 
 namespace gbn {
 
-template <typename T, bool LN, int NV, bool FULL>
+template <typename T, bool LN, int NV, bool FULL, bool RECOMP>
 __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdParams p) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
@@ -108,10 +108,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         while (issued < S && issued < ns) issue();
     }
 
-    // this CTA's saved statistics, staged once
-    for (int i = tid; i < nrows; i += blockDim.x) {
-        st_rstd[i] = p.rstd[row0 + i];
-        if (LN) st_mean[i] = p.mean[row0 + i];
+    // this CTA's saved statistics, staged once (RECOMP: none were saved)
+    if constexpr (!RECOMP) {
+        for (int i = tid; i < nrows; i += blockDim.x) {
+            st_rstd[i] = p.rstd[row0 + i];
+            if (LN) st_mean[i] = p.mean[row0 + i];
+        }
     }
     // gamma: unpacked into registers (kHoldAll), unpacked into shared memory
     // (kHoldX), or kept as raw vectors (kReread)
@@ -154,11 +156,118 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     for (; k < ns; ++k) {
         const bool timed_out = !mbar_wait_bounded(&bar[pos.stage], pos.parity);
         if (timed_out) record_error(p.err, kErrWaitFull);
+        if constexpr (RECOMP && MODE == kHoldAll) {
+            // No saved statistics, row held in registers: x and dy in fp32.
+            // RMSNorm: sum(x^2) and sum(dyhat*x) in one exchange give rstd and
+            // c2 = rstd*sum(dyhat*x)/N.  LayerNorm: sum(x) first (the mean),
+            // then sum((x-mean)^2), sum(dyhat), sum(dyhat*(x-mean)) in one
+            // exchange.  dgamma / dbeta accumulate in pass 2, once rstd is known.
+            const unsigned char *sx = ring + (size_t)pos.stage * stage_bytes + (size_t)ts * 16;
+            float xv[E], dv[E];
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (FULL || ts + j * tpr < nvec) {
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sx + j * vstride), xv + j * V);
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sx + rowb + j * vstride), dv + j * V);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) xv[j * V + e] = dv[j * V + e] = 0.f;
+                }
+            }
+            float mu = 0.f;
+            if constexpr (LN) {
+                float m[1] = {0.f};
+#pragma unroll
+                for (int e = 0; e < E; ++e) m[0] += xv[e];
+                if (slot_reduce<1>(m, red + 6 * kRedStride, flag, timed_out, W, warp, lane, 1 + slot, tpr)) break;
+                mu = m[0] * inv_n;
+            }
+            float r[LN ? 3 : 2];  // sum((x-mean)^2), [sum(dyhat)], sum(dyhat*(x-mean))
+#pragma unroll
+            for (int q = 0; q < (LN ? 3 : 2); ++q) r[q] = 0.f;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const bool live = FULL || ts + j * tpr < nvec;
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float d = live ? xv[j * V + e] - mu : 0.f;
+                    const float dyhat = dv[j * V + e] * gam[j * V + e];
+                    r[0] = fmaf(d, d, r[0]);
+                    if constexpr (LN) r[1] += dyhat;
+                    r[LN ? 2 : 1] = fmaf(dyhat, d, r[LN ? 2 : 1]);
+                }
+            }
+            const bool abort = slot_reduce<LN ? 3 : 2>(r, red + (k & 1) * 3 * kRedStride, flag, LN ? false : timed_out,
+                                                       W, warp, lane, 1 + slot, tpr);
+            if (abort) break;
+            if (ts == 0 && issued < ns) {  // the row is in registers: refill its stage
+                fence_proxy_async();
+                issue();
+            }
+            const float rs = 1.0f / sqrtf(r[0] * inv_n + p.eps);
+            const float a = -rs * (rs * (r[LN ? 2 : 1] * inv_n));
+            const float b = LN ? -rs * (r[1] * inv_n) : 0.f;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (FULL || ts + j * tpr < nvec) {
+                    float o[V];
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float xhat = (xv[j * V + e] - mu) * rs;
+                        const float dyv = dv[j * V + e];
+                        acc_g[j * V + e] = fmaf(dyv, xhat, acc_g[j * V + e]);
+                        if constexpr (LN) acc_b[j * V + e] += dyv;
+                        o[e] = fmaf(dyv * gam[j * V + e], rs, LN ? fmaf(xhat, a, b) : xhat * a);
+                    }
+                    st_global_cs_v4(dxrow + (size_t)j * tpr * V, Tr::pack(o));
+                }
+            }
+            dxrow += row_step;
+            pos.next(S);
+            continue;
+        }
         const int i = slot + k * slots;
-        const float rs = st_rstd[i];
-        const float mu = LN ? st_mean[i] : 0.f;
         const unsigned char *sx = ring + (size_t)pos.stage * stage_bytes + (size_t)ts * 16;
         const unsigned char *sdy = sx + rowb;
+        float rs, mu = 0.f;
+        if constexpr (RECOMP) {
+            // the statistics from the staged row, as the forward forms them:
+            // mean, then the centred squares (LayerNorm), or the mean square
+            float q[1] = {0.f};
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (FULL || ts + j * tpr < nvec) {
+                    float f[V];
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sx + j * vstride), f);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) q[0] = LN ? q[0] + f[e] : fmaf(f[e], f[e], q[0]);
+                }
+            }
+            if (slot_reduce<1>(q, red + 4 * kRedStride, flag, timed_out, W, warp, lane, 1 + slot, tpr)) break;
+            if constexpr (LN) {
+                mu = q[0] * inv_n;
+                float c[1] = {0.f};
+#pragma unroll
+                for (int j = 0; j < NV; ++j) {
+                    if (FULL || ts + j * tpr < nvec) {
+                        float f[V];
+                        Tr::unpack(*reinterpret_cast<const uint4 *>(sx + j * vstride), f);
+#pragma unroll
+                        for (int e = 0; e < V; ++e) {
+                            const float d = f[e] - mu;
+                            c[0] = fmaf(d, d, c[0]);
+                        }
+                    }
+                }
+                slot_reduce<1>(c, red + 5 * kRedStride, flag, false, W, warp, lane, 1 + slot, tpr);
+                rs = 1.0f / sqrtf(c[0] * inv_n + p.eps);
+            } else {
+                rs = 1.0f / sqrtf(q[0] * inv_n + p.eps);
+            }
+        } else {
+            rs = st_rstd[i];
+            mu = LN ? st_mean[i] : 0.f;
+        }
         // pass 1
         float xh[MODE == kHoldAll ? E : 1], dh[HOLD ? E : 1];
         uint4 xraw[MODE == kHoldX ? NV : 1];
@@ -335,8 +444,24 @@ __global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdPar
         const int64_t row = row0 + i;
         const T *xr = static_cast<const T *>(p.x) + row * p.ld_x;
         const T *dyr = static_cast<const T *>(p.dy) + row * p.ld_dy;
-        const float rs = p.rstd[row];
-        const float mu = LN ? p.mean[row] : 0.f;
+        float rs, mu = 0.f;
+        if (p.rstd) {
+            rs = p.rstd[row];
+            mu = LN ? p.mean[row] : 0.f;
+        } else {
+            // no saved statistics: the forward's two passes over the row
+            if (LN) {
+                float t = 0.f;
+                for (int j = threadIdx.x; j < N; j += blockDim.x) t += Tr::load1(xr + j);
+                mu = block_sum(t, sm) * inv_n;
+            }
+            float q = 0.f;
+            for (int j = threadIdx.x; j < N; j += blockDim.x) {
+                const float d = Tr::load1(xr + j) - mu;
+                q = fmaf(d, d, q);
+            }
+            rs = 1.0f / sqrtf(block_sum(q, sm) * inv_n + p.eps);
+        }
         float s1 = 0.f, s2 = 0.f;
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
             const float xhat = (Tr::load1(xr + j) - mu) * rs;
@@ -373,13 +498,21 @@ cudaError_t ensure_smem_optin(K kernel, std::atomic<uint64_t> &done) {
     return e;
 }
 
+template <typename T, bool LN, int NV, bool FULL, bool RECOMP>
+cudaError_t bwd_staged_launch_r(const BwdParams &p, size_t smem, cudaStream_t s) {
+    static std::atomic<uint64_t> done{0};
+    cudaError_t e = ensure_smem_optin(bwd_staged_kernel<T, LN, NV, FULL, RECOMP>, done);
+    if (e != cudaSuccess) return e;
+    bwd_staged_kernel<T, LN, NV, FULL, RECOMP><<<p.G, kRingThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// recompute: no saved statistics (p.rstd == nullptr); the row's statistics
+// are formed from the staged x with p.eps
 template <typename T, bool LN, int NV, bool FULL>
 cudaError_t bwd_staged_launch(const BwdParams &p, size_t smem, cudaStream_t s) {
-    static std::atomic<uint64_t> done{0};
-    cudaError_t e = ensure_smem_optin(bwd_staged_kernel<T, LN, NV, FULL>, done);
-    if (e != cudaSuccess) return e;
-    bwd_staged_kernel<T, LN, NV, FULL><<<p.G, kRingThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return p.rstd ? bwd_staged_launch_r<T, LN, NV, FULL, false>(p, smem, s)
+                  : bwd_staged_launch_r<T, LN, NV, FULL, true>(p, smem, s);
 }
 
 template <typename T, bool LN>

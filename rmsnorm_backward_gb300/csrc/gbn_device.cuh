@@ -242,7 +242,7 @@ __host__ __device__ __forceinline__ void block_rows(int64_t M, int G, int b, int
 
 namespace gbn {
 
-// Floats of reduction scratch per slot and buffer: [NQ <= 2][16 warps].
+// Floats of reduction scratch per slot: 128, as [buffer][NQ][16 warps].
 constexpr int kRedStride = 16;
 
 // Sums the NQ values of every thread of one row slot (W warps, tpr = 32*W

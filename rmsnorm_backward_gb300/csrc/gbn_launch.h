@@ -40,8 +40,8 @@ struct BwdParams {
     const void *dy;
     const void *x;
     const void *gamma;
-    const float *mean;  // LayerNorm only
-    const float *rstd;
+    const float *mean;  // LayerNorm only; nullptr with rstd: recomputed from x
+    const float *rstd;  // nullptr: no saved statistics, recomputed from x with eps
     void *dx;
     float *part;        // [G][ldp] dgamma partials, then [G][ldp] dbeta partials (LayerNorm)
     int64_t M;
@@ -56,6 +56,7 @@ struct BwdParams {
     int64_t ld_x;       // row strides, in elements, of x, dy and dx
     int64_t ld_dy;
     int64_t ld_dx;
+    float eps;          // used when no statistics were saved (rstd == nullptr)
 };
 
 // Shared-memory layout of the staged kernels, computed identically on the

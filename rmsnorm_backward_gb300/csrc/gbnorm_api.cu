@@ -211,13 +211,17 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
     return cuda_status(launch_fwd_plain(dtype, ln, p, stream));
 }
 
+// recompute_eps >= 0: no saved statistics (mean / rstd null), the kernels
+// form them from x with this eps; < 0: the statistics are required.
 int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
                   void *dx, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes_given,
-                  const Opts &o, cudaStream_t stream) {
+                  const Opts &o, cudaStream_t stream, float recompute_eps = -1.f) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (M == 0) return GBN_OK;
-    if (!dy || !x || !gamma || !rstd || !dx || !workspace || (ln && !mean)) return GBN_EINVAL;
+    const bool recompute = recompute_eps >= 0.f;
+    if (!dy || !x || !gamma || !dx || !workspace) return GBN_EINVAL;
+    if (recompute ? (rstd || mean) : (!rstd || (ln && !mean))) return GBN_EINVAL;
     DevInfo d;
     if ((st = device_info(&d)) != GBN_OK) return st;
     if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
@@ -227,6 +231,7 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     p.M = M; p.N = static_cast<int>(N); p.ldp = partial_ld(N); p.G = grid_rows(M, d); p.err = d.err;
     p.l2_hint = env_int("GBN_L2_HINT") != 0;
     p.ld_x = o.ld_x; p.ld_dy = o.ld_dy; p.ld_dx = o.ld_out;
+    p.eps = recompute ? recompute_eps : 0.f;
     const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma) &&
                          stride16(o.ld_x, dtype) && stride16(o.ld_dy, dtype) && stride16(o.ld_out, dtype);
     StagedPlan P;
@@ -325,13 +330,16 @@ int gbn_bwd_reduce(const void *workspace, size_t workspace_bytes, int64_t M, int
 int ln_bwd_ex(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
               void *dgamma, void *dbeta, float eps, int64_t M, int64_t N, int dtype, void *workspace,
               size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream) {
-    (void)eps;
     Opts o;
     int st = check_shape(M, N, dtype);
     if (st == GBN_OK) st = resolve_options(opt, N, dtype, &o);
     if (st != GBN_OK) return st;
     if (M > 0 && (!dgamma || !dbeta)) return GBN_EINVAL;
-    st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream);
+    // no saved statistics: recompute them from x with eps
+    const bool recompute = !mean && !rstd;
+    if (recompute && (!(eps >= 0.f) || !isfinite(eps))) return GBN_EINVAL;
+    st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
+                       recompute ? eps : -1.f);
     if (st != GBN_OK) return st;
     return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, o, stream);
 }
@@ -339,13 +347,16 @@ int ln_bwd_ex(const void *dy, const void *x, const void *gamma, const float *mea
 int rms_bwd_ex(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, void *dgamma,
                float eps, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes,
                const gbn_options *opt, cudaStream_t stream) {
-    (void)eps;
     Opts o;
     int st = check_shape(M, N, dtype);
     if (st == GBN_OK) st = resolve_options(opt, N, dtype, &o);
     if (st != GBN_OK) return st;
     if (M > 0 && !dgamma) return GBN_EINVAL;
-    st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream);
+    // no saved rstd: recompute it from x with eps
+    const bool recompute = !rstd;
+    if (recompute && (!(eps >= 0.f) || !isfinite(eps))) return GBN_EINVAL;
+    st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
+                       recompute ? eps : -1.f);
     if (st != GBN_OK) return st;
     return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, o, stream);
 }
