@@ -16,6 +16,7 @@ measured with CUDA events on the launching stream.  Printed as ONE JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -50,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--reduce", choices=["partials", "atomic", "colwalk"], default="partials",
+                    help="cross-row reduction of dgamma/dbeta: the deterministic default or an ablation")
     ap.add_argument("--stats", choices=["saved", "recompute"], default="saved",
                     help="recompute: the backward gets no saved statistics and forms them from x")
     return ap.parse_args(argv)
@@ -191,7 +194,7 @@ class ClockSampler:
 class Problem:
     """Device buffers and the three launches of one step for a workload."""
 
-    def __init__(self, w: wl.Workload, device, stream, recompute: bool = False):
+    def __init__(self, w: wl.Workload, device, stream, recompute: bool = False, reduce: str = "partials"):
         import rmsnorm_backward_gb300 as gbn
 
         self.gbn = gbn
@@ -242,12 +245,17 @@ class Problem:
                                                    P(self.dgamma), w.eps, M, N, code, P(self.ws), wsb, None, sp))
         self._red = (L.gbn_bwd_reduce, (P(self.ws), wsb, M, N, code, int(w.has_beta), P(self.dgamma),
                                         P(self.dbeta), sp))
+        # the public backward through the options call (contiguous rows,
+        # float32 grads, overwrite, the chosen cross-row reduction)
+        self.opt = gbn.GbnOptions(N, N, N, 0, 0, gbn.REDUCE_MODES[reduce])
+        self.reduce = reduce
+        optp = ctypes.byref(self.opt)
         if w.has_beta:
-            self._bwd = (L.ln_bwd, (P(self.dy), P(self.x), P(self.gamma), P(bmean), P(brstd), P(self.dx),
-                                    P(self.dgamma), P(self.dbeta), beps, M, N, code, P(self.ws), wsb, sp))
+            self._bwd = (L.ln_bwd_ex, (P(self.dy), P(self.x), P(self.gamma), P(bmean), P(brstd), P(self.dx),
+                                       P(self.dgamma), P(self.dbeta), beps, M, N, code, P(self.ws), wsb, optp, sp))
         else:
-            self._bwd = (L.rms_bwd, (P(self.dy), P(self.x), P(self.gamma), P(brstd), P(self.dx),
-                                     P(self.dgamma), beps, M, N, code, P(self.ws), wsb, sp))
+            self._bwd = (L.rms_bwd_ex, (P(self.dy), P(self.x), P(self.gamma), P(brstd), P(self.dx),
+                                        P(self.dgamma), beps, M, N, code, P(self.ws), wsb, optp, sp))
 
     @staticmethod
     def _call(fn_args):
@@ -261,10 +269,10 @@ class Problem:
     def bwd_rows(self):
         # the save-nothing backward has no separate rows phase: time the
         # whole call (rows kernel + reduce) there
-        self._call(self._rows_recompute if self.recompute else self._rows)
+        self._call(self._rows_recompute if self.recompute else (self._bwd if self.reduce != "partials" else self._rows))
 
     def bwd_reduce(self):
-        if not self.recompute:
+        if not self.recompute and self.reduce == "partials":
             self._call(self._red)
 
     def bwd_fused(self):
@@ -433,7 +441,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device)
-    prob = Problem(w, device, stream, recompute=args.stats == "recompute")
+    prob = Problem(w, device, stream, recompute=args.stats == "recompute", reduce=args.reduce)
     flush = L2Flush(device)
     import rmsnorm_backward_gb300 as gbn
 
@@ -483,7 +491,7 @@ def run_ours(args):
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "l2": ("flushed before the forward and before the backward of every step: a 256 MiB write, "
                        "then a 256 MiB read of another buffer so no dirty lines carry into the timed kernel"),
-                "G": G, "staged_kernel": staged, "stats": args.stats,
+                "G": G, "staged_kernel": staged, "stats": args.stats, "reduce": args.reduce,
                 "step": "forward (y, stats) then backward (dx + partial rows, then column reduce)",
                 "timed": ("value = backward minimum bytes / device time of the public backward call (rows kernel "
                           "+ column reduce, CUDA events around the call); roofline = rows kernel alone, own loop"),
@@ -501,8 +509,9 @@ def run_ours(args):
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": ("bwd_staged_kernel (dx + per-CTA partial rows)" if args.stats == "saved" else
-                           "whole save-nothing backward call (rows kernel + column reduce)"),
+                "kernel": ("bwd_staged_kernel (dx + per-CTA partial rows)"
+                           if args.stats == "saved" and args.reduce == "partials" else
+                           "the whole backward call (ablation / save-nothing variant)"),
                 "algorithmic_bytes_per_launch": rows_bytes, "peak_source": peak_src,
             },
             "e2e": {"value": round(world * bwd_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",

@@ -157,13 +157,29 @@ int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
  *   grad_dtype (backward): storage type of dgamma / dbeta: GBN_F32 (the
  *     default) or the dtype of the call (the parameters' own type, the cast
  *     the pages' reduce kernels apply at the end), rounded to nearest even.
+ *   reduce_mode (backward): how dgamma / dbeta are reduced across rows.
+ *     GBN_REDUCE_PARTIALS (0, the default): per-CTA partial rows in the
+ *       workspace, summed per column in a fixed order; deterministic.
+ *     GBN_REDUCE_ATOMIC (1): each CTA adds its partial row into dgamma /
+ *       dbeta with float32 atomics ("Norm backward in Triton", "atomic_add
+ *       straight to a [d] buffer", at CTA granularity); NOT deterministic
+ *       (the order of the additions varies from run to run).  Needs
+ *       grad_dtype GBN_F32.
+ *     GBN_REDUCE_COLWALK (2): a second kernel in which each CTA owns 32
+ *       columns and walks every row of x and dy again ("05: Layer norm",
+ *       kernel ln_bwd_dwdb); deterministic, one more read of x and dy.
+ *       Needs grad_dtype GBN_F32 and the saved statistics.
+ *     The last two exist to measure what the default costs or saves.
  */
+enum { GBN_REDUCE_PARTIALS = 0, GBN_REDUCE_ATOMIC = 1, GBN_REDUCE_COLWALK = 2 };
+
 typedef struct {
     int64_t ld_x;
     int64_t ld_dy;
     int64_t ld_out;
     int accumulate;
     int grad_dtype;
+    int reduce_mode;
 } gbn_options;
 
 /* The four operations with gbn_options; dgamma / dbeta are `void *` of type

@@ -48,7 +48,11 @@ class GbnOptions(ctypes.Structure):
     """gbn_options of include/gbnorm.h."""
 
     _fields_ = [("ld_x", ctypes.c_int64), ("ld_dy", ctypes.c_int64), ("ld_out", ctypes.c_int64),
-                ("accumulate", ctypes.c_int), ("grad_dtype", ctypes.c_int)]
+                ("accumulate", ctypes.c_int), ("grad_dtype", ctypes.c_int), ("reduce_mode", ctypes.c_int)]
+
+
+# reduce_mode values (GBN_REDUCE_* of include/gbnorm.h)
+REDUCE_MODES = {"partials": 0, "atomic": 1, "colwalk": 2}
 
 
 class GbnError(RuntimeError):
@@ -180,8 +184,9 @@ def device_error(clear: bool = True, device=None) -> int:
         return int(lib().gbn_device_error(int(clear)))
 
 
-def _options(ld_x: int, ld_dy: int, ld_out: int, accumulate: bool = False, grad_dtype=torch.float32):
-    return GbnOptions(ld_x, ld_dy, ld_out, int(bool(accumulate)), DTYPE_CODES[grad_dtype])
+def _options(ld_x: int, ld_dy: int, ld_out: int, accumulate: bool = False, grad_dtype=torch.float32,
+             reduce: str = "partials"):
+    return GbnOptions(ld_x, ld_dy, ld_out, int(bool(accumulate)), DTYPE_CODES[grad_dtype], REDUCE_MODES[reduce])
 
 
 def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float, *,
@@ -262,8 +267,12 @@ def _recompute_eps(stats, eps):
 
 def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: Optional[torch.Tensor],
            rstd: Optional[torch.Tensor], *, dx=None, dgamma=None, dbeta=None, workspace=None,
-           accumulate: bool = False, grad_dtype=torch.float32, eps: Optional[float] = None, stream=None):
+           accumulate: bool = False, grad_dtype=torch.float32, eps: Optional[float] = None,
+           reduce: str = "partials", stream=None):
     """LayerNorm backward from the saved mean / rstd. Returns (dx, dgamma, dbeta).
+
+    reduce: "partials" (deterministic, the default), or the measurement
+    ablations "atomic" (nondeterministic) and "colwalk".
 
     With mean = rstd = None nothing was saved: the statistics are formed from
     x with ``eps``.  dgamma / dbeta are float32 unless grad_dtype is x's
@@ -276,7 +285,7 @@ def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: Optiona
     dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
     dbeta = _grads(dbeta, "dbeta", N, grad_dtype, x.device, accumulate)
     workspace, wsb = _workspace(workspace, M, N, x, True)
-    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype)
+    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype, reduce)
     with torch.cuda.device(x.device):
         _check("ln_bwd", lib().ln_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
                                          _ptr(dgamma), _ptr(dbeta), eps_arg, M, N, _code(x), _ptr(workspace), wsb,
@@ -286,7 +295,7 @@ def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: Optiona
 
 def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: Optional[torch.Tensor], *,
             dx=None, dgamma=None, workspace=None, accumulate: bool = False, grad_dtype=torch.float32,
-            eps: Optional[float] = None, stream=None):
+            eps: Optional[float] = None, reduce: str = "partials", stream=None):
     """RMSNorm backward from the saved rstd (None: recomputed from x with eps).
     Returns (dx, dgamma); options as for ln_bwd."""
     if grad_dtype not in (torch.float32, x.dtype):
@@ -295,7 +304,7 @@ def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: Option
     M, N, dx, (ld_x, ld_dy, ld_dx) = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx)
     dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
     workspace, wsb = _workspace(workspace, M, N, x, False)
-    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype)
+    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype, reduce)
     with torch.cuda.device(x.device):
         _check("rms_bwd", lib().rms_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
                                            eps_arg, M, N, _code(x), _ptr(workspace), wsb, ctypes.byref(opt),

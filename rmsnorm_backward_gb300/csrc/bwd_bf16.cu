@@ -9,4 +9,8 @@ cudaError_t launch_bwd_staged_bf16(bool ln, int nv, bool full, const BwdParams &
 
 cudaError_t launch_bwd_plain_bf16(bool ln, const BwdParams &p, cudaStream_t s) { return bwd_plain_dispatch<__nv_bfloat16>(ln, p, s); }
 
+cudaError_t launch_colwalk_bf16(bool ln, const BwdParams &p, float *dg, float *db, bool acc, cudaStream_t s) {
+    return colwalk_dispatch<__nv_bfloat16>(ln, p, dg, db, acc, s);
+}
+
 }  // namespace gbn

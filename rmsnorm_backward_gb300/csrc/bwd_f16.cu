@@ -9,4 +9,8 @@ cudaError_t launch_bwd_staged_f16(bool ln, int nv, bool full, const BwdParams &p
 
 cudaError_t launch_bwd_plain_f16(bool ln, const BwdParams &p, cudaStream_t s) { return bwd_plain_dispatch<__half>(ln, p, s); }
 
+cudaError_t launch_colwalk_f16(bool ln, const BwdParams &p, float *dg, float *db, bool acc, cudaStream_t s) {
+    return colwalk_dispatch<__half>(ln, p, dg, db, acc, s);
+}
+
 }  // namespace gbn

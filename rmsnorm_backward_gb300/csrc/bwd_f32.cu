@@ -9,4 +9,8 @@ cudaError_t launch_bwd_staged_f32(bool ln, int nv, bool full, const BwdParams &p
 
 cudaError_t launch_bwd_plain_f32(bool ln, const BwdParams &p, cudaStream_t s) { return bwd_plain_dispatch<float>(ln, p, s); }
 
+cudaError_t launch_colwalk_f32(bool ln, const BwdParams &p, float *dg, float *db, bool acc, cudaStream_t s) {
+    return colwalk_dispatch<float>(ln, p, dg, db, acc, s);
+}
+
 }  // namespace gbn

@@ -364,8 +364,19 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
 
     // ---- this CTA's partial row(s) --------------------------------------
     const int ldp = p.ldp;
-    float *pg = p.part + (size_t)blockIdx.x * ldp;
-    float *pb = p.part + ((size_t)p.G + blockIdx.x) * ldp;
+    const bool atomic = p.atom_g != nullptr;  // reduction ablation
+    float *pg = atomic ? p.atom_g : p.part + (size_t)blockIdx.x * ldp;
+    float *pb = atomic ? p.atom_b : p.part + ((size_t)p.G + blockIdx.x) * ldp;
+    auto put = [atomic](float *dst, const float4 &v) {
+        if (atomic) {
+            atomicAdd(dst, v.x);
+            atomicAdd(dst + 1, v.y);
+            atomicAdd(dst + 2, v.z);
+            atomicAdd(dst + 3, v.w);
+        } else {
+            *reinterpret_cast<float4 *>(dst) = v;
+        }
+    };
     if (slots == 1) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
@@ -373,11 +384,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
             if (FULL || v < nvec) {
 #pragma unroll
                 for (int e = 0; e < V; e += 4) {
-                    *reinterpret_cast<float4 *>(pg + (size_t)v * V + e) =
-                        make_float4(acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]);
+                    put(pg + (size_t)v * V + e,
+                        make_float4(acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]));
                     if constexpr (LN)
-                        *reinterpret_cast<float4 *>(pb + (size_t)v * V + e) = make_float4(
-                            acc_b[j * V + e], acc_b[j * V + e + 1], acc_b[j * V + e + 2], acc_b[j * V + e + 3]);
+                        put(pb + (size_t)v * V + e, make_float4(acc_b[j * V + e], acc_b[j * V + e + 1],
+                                                                acc_b[j * V + e + 2], acc_b[j * V + e + 3]));
                 }
             }
         }
@@ -408,7 +419,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
                 const float4 b = *reinterpret_cast<const float4 *>(comb + (size_t)s2 * ldp + c);
                 a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
             }
-            *reinterpret_cast<float4 *>(pg + c) = a;
+            put(pg + c, a);
             if constexpr (LN) {
                 const float *cb = comb + (size_t)slots * ldp;
                 float4 d = *reinterpret_cast<const float4 *>(cb + c);
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
                     const float4 b = *reinterpret_cast<const float4 *>(cb + (size_t)s2 * ldp + c);
                     d.x += b.x; d.y += b.y; d.z += b.z; d.w += b.w;
                 }
-                *reinterpret_cast<float4 *>(pb + c) = d;
+                put(pb + c, d);
             }
         }
     }
@@ -481,6 +492,77 @@ __global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdPar
             if (LN) pb[j] += dy;
         }
     }
+    if (p.atom_g) {  // reduction ablation: add the CTA's partial row with atomics
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            atomicAdd(p.atom_g + j, pg[j]);
+            if (LN) atomicAdd(p.atom_b + j, pb[j]);
+        }
+    }
+}
+
+// Reduction ablation after the column-walk design of "05: Layer norm"
+// (kernel ln_bwd_dwdb): CTA b owns columns [32b, 32b + 32) and reads x and
+// dy again, row by row; lane q of row-lane l adds rows l, l+32, ... of
+// column 32b + q in order, then the 32 row-lane sums are added in order.
+// Deterministic; costs a second read of x and dy.
+template <typename T, bool LN, bool ACC>
+__global__ void __launch_bounds__(1024) colwalk_kernel(const BwdParams p, float *__restrict__ dgamma,
+                                                       float *__restrict__ dbeta) {
+    using Tr = Traits<T>;
+    __shared__ float sg[32][33], sb[32][33];
+    const int q = threadIdx.x & 31, lane_row = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + q;
+    float ag = 0.f, ab = 0.f;
+    if (c < p.N) {
+        const T *x = static_cast<const T *>(p.x) + c;
+        const T *dy = static_cast<const T *>(p.dy) + c;
+        int64_t r = lane_row;
+        for (; r + 7 * 32 < p.M; r += 8 * 32) {
+            float xv[8], dv[8], rs[8], mu[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t rr = r + u * 32;
+                xv[u] = Tr::load1(x + rr * p.ld_x);
+                dv[u] = Tr::load1(dy + rr * p.ld_dy);
+                rs[u] = p.rstd[rr];
+                mu[u] = LN ? p.mean[rr] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                ag = fmaf(dv[u], (xv[u] - mu[u]) * rs[u], ag);
+                if (LN) ab += dv[u];
+            }
+        }
+        for (; r < p.M; r += 32) {
+            const float xv = Tr::load1(x + r * p.ld_x), dv = Tr::load1(dy + r * p.ld_dy);
+            ag = fmaf(dv, (xv - (LN ? p.mean[r] : 0.f)) * p.rstd[r], ag);
+            if (LN) ab += dv;
+        }
+    }
+    sg[lane_row][q] = ag;
+    sb[lane_row][q] = ab;
+    __syncthreads();
+    if (lane_row == 0 && c < p.N) {
+        float tg = sg[0][q], tb = sb[0][q];
+        for (int l = 1; l < 32; ++l) {
+            tg += sg[l][q];
+            tb += sb[l][q];
+        }
+        dgamma[c] = ACC ? dgamma[c] + tg : tg;
+        if (LN) dbeta[c] = ACC ? dbeta[c] + tb : tb;
+    }
+}
+
+template <typename T>
+cudaError_t colwalk_dispatch(bool ln, const BwdParams &p, float *dg, float *db, bool acc, cudaStream_t s) {
+    const dim3 grid((p.N + 31) / 32);
+    if (ln)
+        acc ? colwalk_kernel<T, true, true><<<grid, 1024, 0, s>>>(p, dg, db)
+            : colwalk_kernel<T, true, false><<<grid, 1024, 0, s>>>(p, dg, db);
+    else
+        acc ? colwalk_kernel<T, false, true><<<grid, 1024, 0, s>>>(p, dg, db)
+            : colwalk_kernel<T, false, false><<<grid, 1024, 0, s>>>(p, dg, db);
+    return cudaGetLastError();
 }
 
 // Sets the opt-in dynamic shared-memory limit of `kernel` once per device.

@@ -57,6 +57,10 @@ struct BwdParams {
     int64_t ld_dy;
     int64_t ld_dx;
     float eps;          // used when no statistics were saved (rstd == nullptr)
+    // reduction ablation: non-null, the CTA adds its partial row(s) into
+    // these fp32 buffers with atomics instead of storing them in `part`
+    float *atom_g;
+    float *atom_b;
 };
 
 // Shared-memory layout of the staged kernels, computed identically on the
@@ -119,6 +123,11 @@ cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_
 // buffers' previous contents (widened) to the sums before the store
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
                           bool accumulate, cudaStream_t s);
+
+// reduction ablation: dgamma (dbeta) = sum over rows of dy*xhat (dy), each CTA
+// owning 32 columns and walking every row of x and dy in order
+cudaError_t launch_colwalk(int dtype, bool ln, const BwdParams &p, float *dgamma, float *dbeta, bool accumulate,
+                           cudaStream_t s);
 
 // the current device's error flag: its device address, and a synchronising read
 cudaError_t error_flag_address(int **addr);

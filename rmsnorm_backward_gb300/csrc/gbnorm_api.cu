@@ -163,6 +163,7 @@ struct Opts {
     int64_t ld_x = 0, ld_dy = 0, ld_out = 0;
     bool accumulate = false;
     int grad_dtype = GBN_F32;
+    int reduce_mode = GBN_REDUCE_PARTIALS;
 };
 
 int resolve_options(const gbn_options *o, int64_t N, int dtype, Opts *r) {
@@ -174,6 +175,9 @@ int resolve_options(const gbn_options *o, int64_t N, int dtype, Opts *r) {
     r->accumulate = o && o->accumulate == 1;
     r->grad_dtype = o ? o->grad_dtype : GBN_F32;
     if (r->grad_dtype != GBN_F32 && r->grad_dtype != dtype) return GBN_EDTYPE;
+    r->reduce_mode = o ? o->reduce_mode : GBN_REDUCE_PARTIALS;
+    if (r->reduce_mode < GBN_REDUCE_PARTIALS || r->reduce_mode > GBN_REDUCE_COLWALK) return GBN_EINVAL;
+    if (r->reduce_mode != GBN_REDUCE_PARTIALS && r->grad_dtype != GBN_F32) return GBN_EDTYPE;
     return GBN_OK;
 }
 
@@ -215,7 +219,8 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
 // form them from x with this eps; < 0: the statistics are required.
 int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
                   void *dx, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes_given,
-                  const Opts &o, cudaStream_t stream, float recompute_eps = -1.f) {
+                  const Opts &o, cudaStream_t stream, float recompute_eps = -1.f, float *dgamma = nullptr,
+                  float *dbeta = nullptr) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (M == 0) return GBN_OK;
@@ -232,15 +237,23 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     p.l2_hint = env_int("GBN_L2_HINT") != 0;
     p.ld_x = o.ld_x; p.ld_dy = o.ld_dy; p.ld_dx = o.ld_out;
     p.eps = recompute ? recompute_eps : 0.f;
+    if (o.reduce_mode == GBN_REDUCE_ATOMIC) {  // the caller zeroed them, unless accumulating
+        p.atom_g = dgamma;
+        p.atom_b = ln ? dbeta : nullptr;
+    }
     const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma) &&
                          stride16(o.ld_x, dtype) && stride16(o.ld_dy, dtype) && stride16(o.ld_out, dtype);
     StagedPlan P;
     if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
     if (P.ok) {
         p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
-        return cuda_status(launch_bwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
+        st = cuda_status(launch_bwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
+    } else {
+        st = cuda_status(launch_bwd_plain(dtype, ln, p, stream));
     }
-    return cuda_status(launch_bwd_plain(dtype, ln, p, stream));
+    if (st == GBN_OK && o.reduce_mode == GBN_REDUCE_COLWALK)
+        st = cuda_status(launch_colwalk(dtype, ln, p, dgamma, ln ? dbeta : nullptr, o.accumulate, stream));
+    return st;
 }
 
 int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, int64_t N, int dtype, bool ln,
@@ -338,9 +351,15 @@ int ln_bwd_ex(const void *dy, const void *x, const void *gamma, const float *mea
     // no saved statistics: recompute them from x with eps
     const bool recompute = !mean && !rstd;
     if (recompute && (!(eps >= 0.f) || !isfinite(eps))) return GBN_EINVAL;
+    if (recompute && o.reduce_mode == GBN_REDUCE_COLWALK) return GBN_EINVAL;
+    if (M > 0 && o.reduce_mode == GBN_REDUCE_ATOMIC && !o.accumulate) {
+        st = cuda_status(cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream));
+        if (st == GBN_OK) st = cuda_status(cudaMemsetAsync(dbeta, 0, (size_t)N * 4, stream));
+        if (st != GBN_OK) return st;
+    }
     st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
-                       recompute ? eps : -1.f);
-    if (st != GBN_OK) return st;
+                       recompute ? eps : -1.f, static_cast<float *>(dgamma), static_cast<float *>(dbeta));
+    if (st != GBN_OK || (M > 0 && o.reduce_mode != GBN_REDUCE_PARTIALS)) return st;
     return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, o, stream);
 }
 
@@ -355,9 +374,14 @@ int rms_bwd_ex(const void *dy, const void *x, const void *gamma, const float *rs
     // no saved rstd: recompute it from x with eps
     const bool recompute = !rstd;
     if (recompute && (!(eps >= 0.f) || !isfinite(eps))) return GBN_EINVAL;
+    if (recompute && o.reduce_mode == GBN_REDUCE_COLWALK) return GBN_EINVAL;
+    if (M > 0 && o.reduce_mode == GBN_REDUCE_ATOMIC && !o.accumulate) {
+        st = cuda_status(cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream));
+        if (st != GBN_OK) return st;
+    }
     st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
-                       recompute ? eps : -1.f);
-    if (st != GBN_OK) return st;
+                       recompute ? eps : -1.f, static_cast<float *>(dgamma), nullptr);
+    if (st != GBN_OK || (M > 0 && o.reduce_mode != GBN_REDUCE_PARTIALS)) return st;
     return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, o, stream);
 }
 

@@ -57,6 +57,20 @@ cudaError_t launch_bwd_plain_f32(bool, const BwdParams &, cudaStream_t);
 cudaError_t launch_bwd_plain_f16(bool, const BwdParams &, cudaStream_t);
 cudaError_t launch_bwd_plain_bf16(bool, const BwdParams &, cudaStream_t);
 
+cudaError_t launch_colwalk_f32(bool, const BwdParams &, float *, float *, bool, cudaStream_t);
+cudaError_t launch_colwalk_f16(bool, const BwdParams &, float *, float *, bool, cudaStream_t);
+cudaError_t launch_colwalk_bf16(bool, const BwdParams &, float *, float *, bool, cudaStream_t);
+
+cudaError_t launch_colwalk(int dtype, bool ln, const BwdParams &p, float *dgamma, float *dbeta, bool accumulate,
+                           cudaStream_t s) {
+    switch (dtype) {
+        case 0: return launch_colwalk_f32(ln, p, dgamma, dbeta, accumulate, s);
+        case 1: return launch_colwalk_f16(ln, p, dgamma, dbeta, accumulate, s);
+        case 2: return launch_colwalk_bf16(ln, p, dgamma, dbeta, accumulate, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_fwd_staged(int dtype, bool ln, int nv, bool full, const FwdParams &p, size_t smem,
                               cudaStream_t s) {
     switch (dtype) {

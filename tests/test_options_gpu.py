@@ -108,15 +108,17 @@ def test_option_errors():
     g = torch.ones(64, device="cuda", dtype=torch.bfloat16)
     y = torch.empty_like(x)
     r = torch.empty(8, device="cuda")
-    bad_ld = gbn.GbnOptions(32, 0, 0, 0, 0)       # stride below N
-    bad_acc = gbn.GbnOptions(0, 0, 0, 2, 0)       # accumulate not 0/1
-    bad_dt = gbn.GbnOptions(0, 0, 0, 0, 1)        # fp16 grads for bf16 parameters
+    bad_ld = gbn.GbnOptions(32, 0, 0, 0, 0, 0)      # stride below N
+    bad_acc = gbn.GbnOptions(0, 0, 0, 2, 0, 0)      # accumulate not 0/1
+    bad_dt = gbn.GbnOptions(0, 0, 0, 0, 1, 0)       # fp16 grads for bf16 parameters
     s = torch.cuda.current_stream().cuda_stream
     assert L.rms_fwd_ex(x.data_ptr(), g.data_ptr(), y.data_ptr(), r.data_ptr(), 1e-6, 8, 64, 2,
                         ctypes.byref(bad_ld), s) == 1
     ws = torch.empty(gbn.bwd_workspace_bytes(8, 64, torch.bfloat16, False), dtype=torch.uint8, device="cuda")
     dg = torch.empty(64, device="cuda")
-    for opt, code in ((bad_acc, 1), (bad_dt, 2)):
+    bad_mode = gbn.GbnOptions(0, 0, 0, 0, 0, 7)     # unknown reduce mode
+    bad_mode_dt = gbn.GbnOptions(0, 0, 0, 0, 2, 1)  # atomic reduce into bf16 grads
+    for opt, code in ((bad_acc, 1), (bad_dt, 2), (bad_mode, 1), (bad_mode_dt, 2)):
         assert L.rms_bwd_ex(x.data_ptr(), x.data_ptr(), g.data_ptr(), r.data_ptr(), y.data_ptr(), dg.data_ptr(),
                             0.0, 8, 64, 2, ws.data_ptr(), ws.numel(), ctypes.byref(opt), s) == code
     with pytest.raises(ValueError):
