@@ -66,7 +66,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_rms_fwd.argtypes = [_I, _I, _P, _P, ctypes.c_double, _P, _P]
     lib.oracle_ln_bwd.argtypes = [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.oracle_rms_bwd.argtypes = [_I, _I, _P, _P, _P, _P, _P, _P]
-    for f in ("oracle_ln_fwd", "oracle_rms_fwd", "oracle_ln_bwd", "oracle_rms_bwd"):
+    for f in ("oracle_silu_bwd", "oracle_gelu_bwd", "oracle_silu_fwd", "oracle_gelu_fwd"):
+        getattr(lib, f).argtypes = [_I, _P, _P, _P][: 4 if f.endswith("bwd") else 3]
+    for f in ("oracle_ln_fwd", "oracle_rms_fwd", "oracle_ln_bwd", "oracle_rms_bwd", "oracle_silu_bwd",
+              "oracle_gelu_bwd", "oracle_silu_fwd", "oracle_gelu_fwd"):
         getattr(lib, f).restype = None
     return lib
 
@@ -126,3 +129,23 @@ def rms_bwd(dy, x, gamma, rstd, lib: Optional[ctypes.CDLL] = None):
     dx = np.empty((M, N)); dg = np.empty(N)
     lib.oracle_rms_bwd(M, N, _p(dy), _p(x), _p(gamma), _p(rstd), _p(dx), _p(dg))
     return dx, dg
+
+
+def act_bwd(kind: str, dy, preact, lib: Optional[ctypes.CDLL] = None) -> np.ndarray:
+    """dx = dy * f'(preact) for f = SiLU ("silu") or GELU, erf form ("gelu"); any shape."""
+    lib = lib or load()
+    dy, preact = _d(dy), _d(preact)
+    if dy.shape != preact.shape:
+        raise ValueError("dy and preact must have the same shape")
+    dx = np.empty_like(dy)
+    getattr(lib, f"oracle_{kind}_bwd")(dy.size, _p(dy), _p(preact), _p(dx))
+    return dx
+
+
+def act_fwd(kind: str, x, lib: Optional[ctypes.CDLL] = None) -> np.ndarray:
+    """f(x) for f = SiLU or GELU (erf form)."""
+    lib = lib or load()
+    x = _d(x)
+    y = np.empty_like(x)
+    getattr(lib, f"oracle_{kind}_fwd")(x.size, _p(x), _p(y))
+    return y

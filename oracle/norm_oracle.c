@@ -149,3 +149,48 @@ void oracle_rms_bwd(int64_t M, int64_t N, const double *dy, const double *x,
         }
     }
 }
+
+/*
+ * Activation backward, "Norm backward in Triton -- the dγ/dβ reduction",
+ * section "Activation backward -- fuse it into the epilogue" (and "Norm &
+ * activation backward", same section): dx = dy * f'(preact), the derivative
+ * recomputed from the saved pre-activation.
+ *   SiLU: f(x) = x * sigma(x), f'(x) = sigma(x) * (1 + x * (1 - sigma(x))).
+ *   GELU (the pages name it without a formula; the exact erf form is taken):
+ *   f(x) = x * Phi(x), f'(x) = Phi(x) + x * phi(x), Phi the standard normal
+ *   distribution function, phi its density.
+ */
+void oracle_silu_bwd(int64_t n, const double *dy, const double *preact, double *dx)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const double x = preact[i];
+        const double s = 1.0 / (1.0 + exp(-x));
+        dx[i] = dy[i] * (s * (1.0 + x * (1.0 - s)));
+    }
+}
+
+void oracle_gelu_bwd(int64_t n, const double *dy, const double *preact, double *dx)
+{
+    const double inv_sqrt2 = 0.70710678118654752440;
+    const double inv_sqrt2pi = 0.39894228040143267794;
+    for (int64_t i = 0; i < n; ++i) {
+        const double x = preact[i];
+        const double cdf = 0.5 * (1.0 + erf(x * inv_sqrt2));
+        const double pdf = inv_sqrt2pi * exp(-0.5 * x * x);
+        dx[i] = dy[i] * (cdf + x * pdf);
+    }
+}
+
+/* The forwards the backward differentiates (for the oracle's own checks). */
+void oracle_silu_fwd(int64_t n, const double *x, double *y)
+{
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = x[i] / (1.0 + exp(-x[i]));
+}
+
+void oracle_gelu_fwd(int64_t n, const double *x, double *y)
+{
+    const double inv_sqrt2 = 0.70710678118654752440;
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = x[i] * 0.5 * (1.0 + erf(x[i] * inv_sqrt2));
+}

@@ -281,3 +281,36 @@ def pin_rms_is_ln_without_mean(lib):
 
 ALL_PINS = (pin_finite_differences, pin_sympy_exact, pin_torch_fp64, pin_invariants,
             pin_rms_is_ln_without_mean)
+
+
+def pin_activation(lib):
+    """SiLU / GELU backward: finite differences of the forward, exact values,
+    limits, and torch float64 autograd."""
+    import torch
+    import torch.nn.functional as F
+
+    x = np.concatenate([np.linspace(-12, 12, 97), wl.normal(4, 51, 200) * 3])
+    dy = wl.normal(4, 52, x.size)
+    for kind in ("silu", "gelu"):
+        dx = oracle.act_bwd(kind, dy, x, lib=lib)
+        # five-point finite differences of the forward, elementwise
+        h = 1e-3
+        f = lambda t: oracle.act_fwd(kind, t, lib=lib)  # noqa: E731
+        fd = (-f(x + 2 * h) + 8 * f(x + h) - 8 * f(x - h) + f(x - 2 * h)) / (12 * h)
+        _close(dx, dy * fd, 1e-9, f"FD {kind}")
+        # torch autograd in float64
+        xt = torch.tensor(x, requires_grad=True)
+        (F.silu(xt) if kind == "silu" else F.gelu(xt)).backward(torch.tensor(dy))
+        _close(dx, xt.grad.numpy(), 1e-13, f"torch {kind}")
+        # f'(0) = 1/2 for both; f' -> 1 for large x, -> 0 for very negative x
+        one = np.ones(1)
+        _close(oracle.act_bwd(kind, one, np.zeros(1), lib=lib), [0.5], 1e-15, f"{kind}'(0)")
+        _close(oracle.act_bwd(kind, one, np.array([40.0]), lib=lib), [1.0], 1e-12, f"{kind}'(+inf)")
+        _close(oracle.act_bwd(kind, one, np.array([-40.0]), lib=lib), [0.0], 1e-12, f"{kind}'(-inf)")
+    # SiLU has its minimum at x* = -1.27846454276107..., where 1 + x*(1 - sigma(x*)) = 0:
+    # its derivative vanishes there
+    m = oracle.act_bwd("silu", np.ones(1), np.array([-1.2784645427610738]), lib=lib)[0]
+    assert abs(m) < 1e-12, m
+
+
+ALL_PINS = ALL_PINS + (pin_activation,)

@@ -29,3 +29,7 @@ def test_invariants_and_closed_forms(lib):
 
 def test_rms_is_ln_without_the_mean(lib):
     pins.pin_rms_is_ln_without_mean(lib)
+
+
+def test_activation_backward(lib):
+    pins.pin_activation(lib)
