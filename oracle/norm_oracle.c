@@ -158,7 +158,11 @@ void oracle_rms_bwd(int64_t M, int64_t N, const double *dy, const double *x,
  *   SiLU: f(x) = x * sigma(x), f'(x) = sigma(x) * (1 + x * (1 - sigma(x))).
  *   GELU (the pages name it without a formula; the exact erf form is taken):
  *   f(x) = x * Phi(x), f'(x) = Phi(x) + x * phi(x), Phi the standard normal
- *   distribution function, phi its density.
+ *   distribution function, phi its density.  Phi(x) is evaluated as
+ *   erfc(-x / sqrt 2) / 2, its definition through the complementary error
+ *   function: the form (1 + erf(x / sqrt 2)) / 2 cancels to no correct digit
+ *   in double below x = -8, where Phi is still far from negligible next to
+ *   x * phi(x).
  */
 void oracle_silu_bwd(int64_t n, const double *dy, const double *preact, double *dx)
 {
@@ -175,7 +179,7 @@ void oracle_gelu_bwd(int64_t n, const double *dy, const double *preact, double *
     const double inv_sqrt2pi = 0.39894228040143267794;
     for (int64_t i = 0; i < n; ++i) {
         const double x = preact[i];
-        const double cdf = 0.5 * (1.0 + erf(x * inv_sqrt2));
+        const double cdf = 0.5 * erfc(-x * inv_sqrt2);
         const double pdf = inv_sqrt2pi * exp(-0.5 * x * x);
         dx[i] = dy[i] * (cdf + x * pdf);
     }
@@ -192,5 +196,5 @@ void oracle_gelu_fwd(int64_t n, const double *x, double *y)
 {
     const double inv_sqrt2 = 0.70710678118654752440;
     for (int64_t i = 0; i < n; ++i)
-        y[i] = x[i] * 0.5 * (1.0 + erf(x[i] * inv_sqrt2));
+        y[i] = x[i] * 0.5 * erfc(-x[i] * inv_sqrt2);
 }

@@ -307,6 +307,26 @@ def pin_activation(lib):
         _close(oracle.act_bwd(kind, one, np.zeros(1), lib=lib), [0.5], 1e-15, f"{kind}'(0)")
         _close(oracle.act_bwd(kind, one, np.array([40.0]), lib=lib), [1.0], 1e-12, f"{kind}'(+inf)")
         _close(oracle.act_bwd(kind, one, np.array([-40.0]), lib=lib), [0.0], 1e-12, f"{kind}'(-inf)")
+    # lower tails, relative to closed forms that use neither erf nor the oracle's sigma:
+    # GELU'(x) = phi(x) (Phi(x) / phi(x) - |x|), with Mills' ratio Phi(x) / phi(x)
+    # = (1/|x|) sum_k (-1)^k (2k-1)!! / x^(2k) (asymptotic; summed to its smallest term)
+    for t in (-9.0, -12.0, -16.0, -20.0, -25.0, -30.0, -35.0):
+        term, mills, k = 1.0, 0.0, 0
+        while True:
+            mills += term
+            nxt = -term * (2 * k + 1) / (t * t)
+            if abs(nxt) >= abs(term) or abs(nxt) < 1e-18:
+                break
+            term, k = nxt, k + 1
+        pdf = np.exp(-0.5 * t * t) / np.sqrt(2.0 * np.pi)
+        want = pdf * (mills / abs(t) - abs(t))
+        got = oracle.act_bwd("gelu", np.ones(1), np.array([t]), lib=lib)[0]
+        assert abs(got - want) <= 1e-12 * abs(want), ("GELU' lower tail", t, got, want)
+        # sigma(x) = e^x - e^(2x) + O(e^(3x)) gives, as x -> -inf,
+        # SiLU'(x) = e^x (1 + x) - e^(2x) (1 + 2x) + O(x e^(3x))
+        want = np.exp(t) * (1.0 + t) - np.exp(2.0 * t) * (1.0 + 2.0 * t)
+        got = oracle.act_bwd("silu", np.ones(1), np.array([t]), lib=lib)[0]
+        assert abs(got - want) <= 1e-7 * abs(want), ("SiLU' lower tail", t, got, want)
     # SiLU has its minimum at x* = -1.27846454276107..., where 1 + x*(1 - sigma(x*)) = 0:
     # its derivative vanishes there
     m = oracle.act_bwd("silu", np.ones(1), np.array([-1.2784645427610738]), lib=lib)[0]

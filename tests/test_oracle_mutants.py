@@ -35,7 +35,9 @@ MUTANTS = [
     ("ln y missing beta", "y[r * N + j] = gamma[j] * xhat + beta[j];", "y[r * N + j] = gamma[j] * xhat;", 0),
     ("silu derivative missing the x term", "dx[i] = dy[i] * (s * (1.0 + x * (1.0 - s)));", "dx[i] = dy[i] * s;", 0),
     ("gelu derivative missing the pdf term", "dx[i] = dy[i] * (cdf + x * pdf);", "dx[i] = dy[i] * cdf;", 0),
-    ("gelu erf argument unscaled", "const double cdf = 0.5 * (1.0 + erf(x * inv_sqrt2));", "const double cdf = 0.5 * (1.0 + erf(x));", 0),
+    ("gelu erfc argument unscaled", "const double cdf = 0.5 * erfc(-x * inv_sqrt2);", "const double cdf = 0.5 * erfc(-x);", 0),
+    ("gelu distribution function through 1 + erf (lower-tail cancellation)",
+     "const double cdf = 0.5 * erfc(-x * inv_sqrt2);", "const double cdf = 0.5 * (1.0 + erf(x * inv_sqrt2));", 0),
     ("ln c2 divided by N-1", "const double mean_dyhat_xhat = s2 / (double)N;\n        for (int64_t j = 0; j < N; ++j) {\n            const double xhat = (xr[j] - mu) * rs;",
      "const double mean_dyhat_xhat = s2 / (double)(N + 1);\n        for (int64_t j = 0; j < N; ++j) {\n            const double xhat = (xr[j] - mu) * rs;", 0),
 ]
