@@ -12,6 +12,7 @@ measured with CUDA events on the launching stream.  Printed as ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the float64 CPU oracle, timed on host cores
+    python bench.py --activation silu|gelu  # the activation backward dx = dy * f'(preact)
 """
 from __future__ import annotations
 
@@ -55,6 +56,8 @@ def parse_args(argv=None):
                     help="cross-row reduction of dgamma/dbeta: the deterministic default or an ablation")
     ap.add_argument("--stats", choices=["saved", "recompute"], default="saved",
                     help="recompute: the backward gets no saved statistics and forms them from x")
+    ap.add_argument("--activation", choices=["silu", "gelu"], default=None,
+                    help="time the activation backward on a 16384 x 4096 bf16 tensor instead of the norm")
     return ap.parse_args(argv)
 
 
@@ -100,28 +103,35 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of every CUDA source of the library (a traffic record taken from
-    an ncu capture is only valid for the sources it was captured from)."""
-    import glob
+# the sources each captured kernel is built from
+KERNEL_SOURCES = {
+    "bwd_staged_kernel": ("gbn_device.cuh", "gbn_launch.h", "bwd_kernels.cuh", "bwd_f32.cu", "bwd_f16.cu",
+                          "bwd_bf16.cu"),
+    "act_bwd_kernel": ("gbn_device.cuh", "gbn_launch.h", "act_bwd.cu"),
+}
 
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the CUDA sources one kernel is built from (a traffic record
+    taken from an ncu capture is only valid for the sources it was captured
+    from)."""
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(ROOT, "rmsnorm_backward_gb300", "csrc", "*"))):
-        with open(path, "rb") as f:
-            h.update(os.path.basename(path).encode())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "rmsnorm_backward_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the fused backward kernel from an ncu capture,
-    if the capture was taken of the current kernel source."""
+    """DRAM bytes per launch of a workload's dominant kernel from an ncu
+    capture, if the capture was taken of that kernel's current sources."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f).get(workload)
+        if not rec or rec.get("source_hash") != kernel_source_hash(rec["kernel"]):
+            return None
     except Exception:
-        return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -575,9 +585,174 @@ def run_reference(args):
     }), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# activation backward: dx = dy * f'(preact)
+# ---------------------------------------------------------------------------
+ACT_METRIC = "activation bwd (dx = dy * f'(preact)) achieved HBM GB/s at M×N"
+
+
+def act_cpu_baseline(a, target_s: float = 10.0):
+    import oracle
+
+    n = min(a.n, 1 << 22)
+    inp = wl.make_act_inputs(a.with_shape(1, n))
+    d, p = wl.exact_double(inp["dy"]).reshape(-1), wl.exact_double(inp["preact"]).reshape(-1)
+    calls, t_total = 0, 0.0
+    while t_total < target_s:
+        t0 = time.perf_counter()
+        oracle.act_bwd(a.kind, d, p)
+        t_total += time.perf_counter() - t0
+        calls += 1
+    per_call = t_total / calls
+    return {"value": round(wl.act_min_bytes(a.dtype, n) / per_call / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (f"float64 oracle {a.kind} backward (C, one thread) on the first {n} of {a.n} elements "
+                       f"of {a.name}, {calls} calls, {t_total:.1f} s; GB/s counts the {a.dtype} bytes")}
+
+
+def run_activation(args):
+    rank, world, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import rmsnorm_backward_gb300 as gbn
+
+    a = wl.ACT_WORKLOADS[f"{args.activation}_bf16_16384x4096"]
+    inp = wl.make_act_inputs(a)
+    dy, pre = inp["dy"].to(device), inp["preact"].to(device)
+    dx = torch.empty_like(dy)
+    stream = torch.cuda.Stream(device)
+    flush = L2Flush(device)
+    L = gbn.lib()
+    fn = getattr(L, f"{a.kind}_bwd")
+    code = gbn.DTYPE_CODES[dy.dtype]
+    call_args = (dy.data_ptr(), pre.data_ptr(), dx.data_ptr(), a.n, code, stream.cuda_stream)
+
+    def step():
+        st = fn(*call_args)
+        if st != 0:
+            raise RuntimeError(f"{a.kind}_bwd returned status {st}")
+
+    K = args.steps
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush()
+            step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index, enabled=not args.no_clocks) as clk:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for e in ev:
+                flush()
+                e[0].record(stream)
+                step()
+                e[1].record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    times = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    t_s = dist_max(float(times.sum()) / 1e3, world, device)
+    nbytes = wl.act_min_bytes(a.dtype, a.n)
+    value = world * K * nbytes / t_s / 1e9
+    peak, peak_src = measured_hbm_peak()
+    avg = t_s / K
+    # end to end through the public binding: pinned host dy, preact in; dx out
+    h_dy, h_pre = inp["dy"].pin_memory(), inp["preact"].pin_memory()
+    h_dx = torch.empty_like(h_dy).pin_memory()
+
+    def one():
+        with torch.cuda.stream(stream):
+            dy.copy_(h_dy, non_blocking=True)
+            pre.copy_(h_pre, non_blocking=True)
+            getattr(gbn, f"{a.kind}_bwd")(dy, pre, dx=dx, stream=stream)
+            h_dx.copy_(dx, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        one()
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1) / args.e2e_steps, world, device)
+    if gbn.device_error(clear=True, device=device):
+        raise SystemExit("kernel error flag set")
+    if rank == 0:
+        out = {
+            "metric": ACT_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(avg * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": a.dtype, "data": "synthetic",
+            "config": {"workload": a.name, "op": f"{a.kind} backward", "M": a.M, "N": a.N,
+                       "inputs": wl.ACT_RECIPE, "seed": a.seed,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed before every launch (256 MiB write, then a 256 MiB read)",
+                       "timed": "CUDA events around each act_bwd launch on its stream"},
+            "us": round(avg * 1e6, 3),
+            "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / avg / 1e9, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(nbytes / avg / 1e9 / peak, 4), "traffic": recorded_traffic(a.name),
+                         "kernel": "act_bwd_kernel", "algorithmic_bytes_per_launch": nbytes,
+                         "peak_source": peak_src},
+            "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": 2 * a.n * wl.ELEM_BYTES[a.dtype],
+                    "d2h_bytes_per_step": a.n * wl.ELEM_BYTES[a.dtype], "ms_per_step": round(e2e_ms, 4),
+                    "what": f"pinned host -> device dy, preact; {a.kind}_bwd; device -> pinned host dx"},
+            "gpu_launches": K,
+            "clocks": clk.summary(),
+            "wall_s_timed_region": round(wall, 3),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = act_cpu_baseline(a)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_act_reference(args):
+    """The float64 oracle's activation backward as the reference arm (rank 0 only)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+
+    a = wl.ACT_WORKLOADS[f"{args.activation}_bf16_16384x4096"]
+    n = min(a.n, 1 << 20)
+    inp = wl.make_act_inputs(a.with_shape(1, n))
+    d, p = wl.exact_double(inp["dy"]).reshape(-1), wl.exact_double(inp["preact"]).reshape(-1)
+    for _ in range(args.warmup):
+        oracle.act_bwd(a.kind, d, p)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.act_bwd(a.kind, d, p)
+    dt = time.perf_counter() - t0
+    value = args.steps * wl.act_min_bytes(a.dtype, n) / dt / 1e9
+    sample = (f"float64 oracle {a.kind} backward (C, one thread) on the first {n} of {a.n} elements of "
+              f"{a.name} per step; GB/s counts the {a.dtype} bytes of those elements")
+    print(json.dumps({
+        "impl": "reference", "metric": ACT_METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": a.name, "M": a.M, "N": a.N, "sample_elements": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.activation and args.impl == "reference":
+        run_act_reference(args)
+    elif args.activation:
+        run_activation(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

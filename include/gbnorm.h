@@ -262,6 +262,19 @@ int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G,
                  int *staged);
 
 /*
+ * Activation backward ("Norm backward in Triton", section "Activation
+ * backward -- fuse it into the epilogue"): dx = dy * f'(preact), the
+ * derivative recomputed from the saved pre-activation, for
+ *   silu_bwd: f'(x) = sigma(x) * (1 + x * (1 - sigma(x))),
+ *   gelu_bwd: the exact (erf) GELU, f'(x) = Phi(x) + x * phi(x).
+ *   dy, preact (in), dx (out): n contiguous elements of `dtype`, device
+ *   memory; dx may alias dy.  Float32 arithmetic, dx rounded to nearest
+ *   even.  n = 0 is a no-op.
+ */
+int silu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype, cudaStream_t stream);
+int gelu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype, cudaStream_t stream);
+
+/*
  * Every wait inside the library's kernels (on a shared-memory barrier that
  * a bulk copy completes) gives up after about two seconds; the kernel then
  * records an error code in a per-device flag, drains its own copies with

@@ -79,12 +79,14 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ln_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, opt, _vp]
     L.rms_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, opt, _vp]
     L.gbn_bwd_plan.argtypes = [_i64, _i64, _int, _int, ctypes.POINTER(_int), ctypes.POINTER(_int)]
+    L.silu_bwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
+    L.gelu_bwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
     L.gbn_device_error.argtypes = [_int]
     L.gbn_status_string.argtypes = [_int]
     L.gbn_status_string.restype = ctypes.c_char_p
     for name in ("ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd", "ln_fwd_ex", "rms_fwd_ex", "ln_bwd_ex", "rms_bwd_ex",
                  "ln_bwd_rows", "rms_bwd_rows",
-                 "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error"):
+                 "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error", "silu_bwd", "gelu_bwd"):
         getattr(L, name).restype = _int
     return L
 
@@ -348,3 +350,29 @@ def bwd_reduce(workspace: torch.Tensor, M: int, N: int, dtype: torch.dtype, has_
         _check("gbn_bwd_reduce", lib().gbn_bwd_reduce(
             _ptr(workspace), workspace.numel() * workspace.element_size(), M, N, DTYPE_CODES[dtype],
             int(has_beta), _ptr(dgamma), _ptr(dbeta) if has_beta else None, _stream(dev, stream)))
+
+
+def _act_bwd(fn: str, dy: torch.Tensor, preact: torch.Tensor, dx: Optional[torch.Tensor], stream):
+    if not (dy.is_contiguous() and preact.is_contiguous()):
+        raise ValueError(f"{fn}: dy and preact must be contiguous")
+    if dy.shape != preact.shape or dy.dtype != preact.dtype or dy.device != preact.device:
+        raise ValueError(f"{fn}: dy and preact must match in shape, dtype and device")
+    code = _code(dy)
+    if dx is None:
+        dx = torch.empty_like(dy)
+    elif not dx.is_contiguous() or dx.shape != dy.shape or dx.dtype != dy.dtype or dx.device != dy.device:
+        raise ValueError(f"{fn}: dx must be a contiguous tensor like dy")
+    dev = dy.device
+    with torch.cuda.device(dev):
+        _check(fn, getattr(lib(), fn)(_ptr(dy), _ptr(preact), _ptr(dx), dy.numel(), code, _stream(dev, stream)))
+    return dx
+
+
+def silu_bwd(dy: torch.Tensor, preact: torch.Tensor, *, dx: Optional[torch.Tensor] = None, stream=None):
+    """dx = dy * SiLU'(preact), elementwise; ``dx`` may be ``dy`` (in place)."""
+    return _act_bwd("silu_bwd", dy, preact, dx, stream)
+
+
+def gelu_bwd(dy: torch.Tensor, preact: torch.Tensor, *, dx: Optional[torch.Tensor] = None, stream=None):
+    """dx = dy * GELU'(preact) (exact erf form), elementwise; ``dx`` may be ``dy``."""
+    return _act_bwd("gelu_bwd", dy, preact, dx, stream)

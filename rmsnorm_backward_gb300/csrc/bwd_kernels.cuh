@@ -566,20 +566,6 @@ cudaError_t colwalk_dispatch(bool ln, const BwdParams &p, float *dg, float *db, 
 }
 
 // Sets the opt-in dynamic shared-memory limit of `kernel` once per device.
-template <typename K>
-cudaError_t ensure_smem_optin(K kernel, std::atomic<uint64_t> &done) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 64 && ((done.load(std::memory_order_acquire) >> dev) & 1u)) return cudaSuccess;
-    int optin = 0;
-    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e == cudaSuccess && dev < 64) done.fetch_or(uint64_t(1) << dev, std::memory_order_release);
-    return e;
-}
-
 template <typename T, bool LN, int NV, bool FULL, bool RECOMP>
 cudaError_t bwd_staged_launch_r(const BwdParams &p, size_t smem, cudaStream_t s) {
     static std::atomic<uint64_t> done{0};

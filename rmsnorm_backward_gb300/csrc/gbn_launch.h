@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -128,6 +130,34 @@ cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma
 // owning 32 columns and walking every row of x and dy in order
 cudaError_t launch_colwalk(int dtype, bool ln, const BwdParams &p, float *dgamma, float *dbeta, bool accumulate,
                            cudaStream_t s);
+
+// opts a kernel into the device's full dynamic shared memory, once per device
+template <typename K>
+cudaError_t ensure_smem_optin(K kernel, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && ((done.load(std::memory_order_acquire) >> dev) & 1u)) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess && dev < 64) done.fetch_or(uint64_t(1) << dev, std::memory_order_release);
+    return e;
+}
+
+// activation backward dx = dy * f'(preact) over n contiguous elements
+enum : int { kActSilu = 0, kActGelu = 1 };
+struct ActParams {
+    const void *dy, *pre;
+    void *dx;
+    int64_t n;
+    int64_t nchunks;  // full chunks of the kernel's shape (0 when a pointer is unaligned)
+    int vec_ok;
+    int *err;
+};
+cudaError_t launch_act_bwd(int act, int dtype, const void *dy, const void *pre, void *dx, int64_t n, int sms,
+                           int *err, cudaStream_t s);
 
 // the current device's error flag: its device address, and a synchronising read
 cudaError_t error_flag_address(int **addr);

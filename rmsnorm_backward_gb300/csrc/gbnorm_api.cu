@@ -398,6 +398,25 @@ int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
                       stream);
 }
 
+int act_bwd_impl(int act, const void *dy, const void *preact, void *dx, int64_t n, int dtype, cudaStream_t s) {
+    if (!valid_dtype(dtype)) return GBN_EDTYPE;
+    if (n < 0) return GBN_EINVAL;
+    if (n == 0) return GBN_OK;
+    if (!dy || !preact || !dx) return GBN_EINVAL;
+    DevInfo d;
+    int st = device_info(&d);
+    if (st != GBN_OK) return st;
+    return cuda_status(launch_act_bwd(act, dtype, dy, preact, dx, n, d.sms, d.err, s));
+}
+
+int silu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype, cudaStream_t stream) {
+    return act_bwd_impl(kActSilu, dy, preact, dx, n, dtype, stream);
+}
+
+int gelu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype, cudaStream_t stream) {
+    return act_bwd_impl(kActGelu, dy, preact, dx, n, dtype, stream);
+}
+
 int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *staged) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;

@@ -63,3 +63,15 @@ def test_host_side_argument_checks(lib):
     assert L.rms_fwd(None, None, None, None, 1e-5, 0, 8, 2, None) == 0
     assert L.gbn_bwd_workspace_bytes(0, 8, 2, 0) == 0
     assert L.gbn_bwd_workspace_bytes(4, 8, 9, 0) == 0
+
+
+def test_activation_host_checks(lib):
+    import rmsnorm_backward_gb300 as gbn
+    L = gbn._declare(ctypes.CDLL(gbn.library_path))
+    p = ctypes.c_void_p(16)
+    for fn in (L.silu_bwd, L.gelu_bwd):
+        assert fn(p, p, p, 0, 2, None) == 0       # empty: no-op, no device needed
+        assert fn(None, p, p, 8, 2, None) == 1    # null pointer
+        assert fn(p, p, None, 8, 2, None) == 1
+        assert fn(p, p, p, -1, 2, None) == 1      # negative size
+        assert fn(p, p, p, 8, 5, None) == 2       # unknown dtype

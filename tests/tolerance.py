@@ -66,8 +66,10 @@ class Report:
                 f"at {self.worst_index}")
 
 
-def check_elementwise(name: str, got: np.ndarray, ref: np.ndarray, dtype: str, scale_row: np.ndarray) -> Report:
-    """got, ref: [M, N] (got already widened to float64); scale_row: [M]."""
+def check_elementwise(name: str, got: np.ndarray, ref: np.ndarray, dtype: str, scale_row: np.ndarray,
+                      abs_floor=0.0) -> Report:
+    """got, ref: [M, N] (got already widened to float64); scale_row: [M];
+    abs_floor: an extra absolute allowance (scalar or broadcastable to [M, N])."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     A = np.ldexp(np.asarray(scale_row, dtype=np.float64), A_EXP)[:, None]
@@ -78,7 +80,7 @@ def check_elementwise(name: str, got: np.ndarray, ref: np.ndarray, dtype: str, s
         R = round_to(ref, dtype)
         strict = 2.0 * ulp(R, dtype)
         err = np.abs(got - R)
-    allowed = np.maximum(strict, A)
+    allowed = np.maximum(np.maximum(strict, A), abs_floor)
     bad = ~(err <= allowed)  # NaN counts as bad
     ratio = np.where(allowed > 0, err / np.where(allowed > 0, allowed, 1), np.where(err > 0, np.inf, 0))
     ratio = np.where(np.isnan(ratio), np.inf, ratio)
@@ -136,3 +138,30 @@ def y_scale(op: str, x, gamma, beta, mean, rstd, chunk: int = 1024) -> np.ndarra
             t = t + np.abs(beta)[None, :]
         out[r0:r1] = t.max(axis=1)
     return out
+
+
+def check_activation(name: str, got, ref, dtype: str, kind: str, dy, preact) -> Report:
+    """dx = dy * f'(preact), elementwise (all arrays flat, float64).
+
+    The term scale of an element is |dy| times the sum of the magnitudes of the
+    terms that form f': SiLU  sigma(x) (1 + |x| (1 - sigma(x)));  GELU
+    Phi(x) + |x| phi(x).  The A floor covers the cancellation at the zeros of
+    f'.  An extra absolute floor 2**-149 (1 + |dy| (1 + |x|)) covers a float32
+    intermediate that is subnormal (e^-|x| or phi(x) far in the tail, whose
+    absolute error is one subnormal quantum, scaled by the factors after it).
+    """
+    from scipy.special import expit, ndtr
+
+    x = np.asarray(preact, dtype=np.float64).reshape(-1)
+    d = np.abs(np.asarray(dy, dtype=np.float64).reshape(-1))
+    ax = np.abs(x)
+    if kind == "silu":
+        sg = expit(x)
+        t = sg * (1.0 + ax * expit(-x))
+    else:
+        t = ndtr(x) + ax * np.exp(-0.5 * np.minimum(ax, 40.0) ** 2) / np.sqrt(2.0 * np.pi)
+    scale = d * t
+    floor = 2.0 ** -149 * (1.0 + d * (1.0 + ax))
+    return check_elementwise(name, np.asarray(got, dtype=np.float64).reshape(-1, 1),
+                             np.asarray(ref, dtype=np.float64).reshape(-1, 1), dtype, scale,
+                             floor.reshape(-1, 1))

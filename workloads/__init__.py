@@ -50,6 +50,8 @@ STREAM_BETA = 4
 STREAM_ROW_SHIFT = 5
 STREAM_ROW_SCALE = 6
 STREAM_OUTLIER_COLS = 7
+STREAM_PREACT = 8
+STREAM_ACT_DY = 9
 
 _CHUNK = 1 << 22
 
@@ -228,3 +230,51 @@ def fwd_min_bytes(op: str, dtype: str, M: int, N: int) -> int:
     nstat = 2 if op == "ln" else 1
     nparam = 2 if op == "ln" else 1
     return 2 * M * N * es + nparam * N * es + 4 * nstat * M
+
+
+# ---------------------------------------------------------------------------
+# activation backward inputs: dy and the saved pre-activation of an MLP's
+# SiLU / GELU ("Norm backward in Triton", section "Activation backward")
+# ---------------------------------------------------------------------------
+ACT_RECIPE = "preact = 2 N(0,1) (both tails and the zeros of f' are covered); dy = N(0,1)"
+
+
+@dataclasses.dataclass(frozen=True)
+class ActWorkload:
+    """dx = dy * f'(preact) over an M x N activation tensor (stored contiguous)."""
+
+    name: str
+    kind: str  # "silu" | "gelu"
+    dtype: str
+    M: int
+    N: int
+    seed: int = 0
+
+    @property
+    def n(self) -> int:
+        return self.M * self.N
+
+    def with_shape(self, M: int, N: int) -> "ActWorkload":
+        return dataclasses.replace(self, M=M, N=N, name=f"{self.name}@{M}x{N}")
+
+
+ACT_WORKLOADS: Dict[str, ActWorkload] = {
+    a.name: a
+    for a in (
+        ActWorkload("silu_bf16_16384x4096", "silu", "bf16", 16384, 4096),
+        ActWorkload("gelu_bf16_16384x4096", "gelu", "bf16", 16384, 4096),
+    )
+}
+
+
+def make_act_inputs(a: ActWorkload) -> Dict[str, torch.Tensor]:
+    """Storage-dtype CPU tensors ``dy`` and ``preact`` of shape [M, N]."""
+    return {
+        "dy": to_storage(normal(a.seed, STREAM_ACT_DY, a.n).reshape(a.M, a.N), a.dtype),
+        "preact": to_storage(2.0 * normal(a.seed, STREAM_PREACT, a.n).reshape(a.M, a.N), a.dtype),
+    }
+
+
+def act_min_bytes(dtype: str, n: int) -> int:
+    """Algorithmic HBM bytes of one activation backward: read dy and preact, write dx."""
+    return 3 * n * ELEM_BYTES[dtype]
