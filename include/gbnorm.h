@@ -281,7 +281,8 @@ int gelu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype,
  * another bounded wait and returns instead of hanging.  This call
  * synchronises the current device, returns the flag (0 = no error) and, if
  * clear != 0, resets it.  GBN_ECUDA (as a negative number) if the
- * synchronisation or the read fails.
+ * synchronisation or the read fails.  Codes: 1 a bulk copy did not
+ * complete; 2 copies still in flight when the kernel gave up draining them.
  */
 int gbn_device_error(int clear);
 

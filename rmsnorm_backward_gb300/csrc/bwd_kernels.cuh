@@ -39,6 +39,87 @@
 
 namespace gbn {
 
+// This CTA's partial row(s) of dgamma / dbeta from the threads' register
+// accumulators (a thread owns vectors ts, ts + tpr, ...).  Several slots add
+// their accumulators in slot order in shared memory (`comb`, the ring area,
+// free once every slot is done with its stages).  With p.atom_g set (the
+// atomics ablation) the sums go into dgamma / dbeta with fp32 atomics.
+template <typename T, bool LN, int NV, bool FULL>
+__device__ __forceinline__ void bwd_store_partials(const BwdParams &p, const float *acc_g, const float *acc_b,
+                                                   unsigned char *comb_area, int slots, int slot, int ts, int tpr,
+                                                   int nvec) {
+    constexpr int V = Traits<T>::kVec;
+    const int tid = threadIdx.x;
+    const int N = p.N;
+    const int ldp = p.ldp;
+    const bool atomic = p.atom_g != nullptr;  // reduction ablation
+    float *pg = atomic ? p.atom_g : p.part + (size_t)blockIdx.x * ldp;
+    float *pb = atomic ? p.atom_b : p.part + ((size_t)p.G + blockIdx.x) * ldp;
+    auto put = [atomic](float *dst, const float4 &v) {
+        if (atomic) {
+            atomicAdd(dst, v.x);
+            atomicAdd(dst + 1, v.y);
+            atomicAdd(dst + 2, v.z);
+            atomicAdd(dst + 3, v.w);
+        } else {
+            *reinterpret_cast<float4 *>(dst) = v;
+        }
+    };
+    if (slots == 1) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int v = ts + j * tpr;
+            if (FULL || v < nvec) {
+#pragma unroll
+                for (int e = 0; e < V; e += 4) {
+                    put(pg + (size_t)v * V + e,
+                        make_float4(acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]));
+                    if constexpr (LN)
+                        put(pb + (size_t)v * V + e, make_float4(acc_b[j * V + e], acc_b[j * V + e + 1],
+                                                                acc_b[j * V + e + 2], acc_b[j * V + e + 3]));
+                }
+            }
+        }
+    } else {
+        __syncthreads();  // every slot is done with its ring stages
+        float *comb = reinterpret_cast<float *>(comb_area);
+        float *comb_g = comb + (size_t)slot * ldp;
+        float *comb_b = comb + ((size_t)slots + slot) * ldp;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int v = ts + j * tpr;
+            if (FULL || v < nvec) {
+#pragma unroll
+                for (int e = 0; e < V; e += 4) {
+                    *reinterpret_cast<float4 *>(comb_g + (size_t)v * V + e) = make_float4(
+                        acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]);
+                    if constexpr (LN)
+                        *reinterpret_cast<float4 *>(comb_b + (size_t)v * V + e) = make_float4(
+                            acc_b[j * V + e], acc_b[j * V + e + 1], acc_b[j * V + e + 2], acc_b[j * V + e + 3]);
+                }
+            }
+        }
+        __syncthreads();
+        for (int c = tid * 4; c < N; c += blockDim.x * 4) {
+            float4 a = *reinterpret_cast<const float4 *>(comb + c);
+            for (int s2 = 1; s2 < slots; ++s2) {
+                const float4 b = *reinterpret_cast<const float4 *>(comb + (size_t)s2 * ldp + c);
+                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+            }
+            put(pg + c, a);
+            if constexpr (LN) {
+                const float *cb = comb + (size_t)slots * ldp;
+                float4 d = *reinterpret_cast<const float4 *>(cb + c);
+                for (int s2 = 1; s2 < slots; ++s2) {
+                    const float4 b = *reinterpret_cast<const float4 *>(cb + (size_t)s2 * ldp + c);
+                    d.x += b.x; d.y += b.y; d.z += b.z; d.w += b.w;
+                }
+                put(pb + c, d);
+            }
+        }
+    }
+}
+
 template <typename T, bool LN, int NV, bool FULL, bool RECOMP>
 __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdParams p) {
     using Tr = Traits<T>;
@@ -362,75 +443,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         }
     }
 
-    // ---- this CTA's partial row(s) --------------------------------------
-    const int ldp = p.ldp;
-    const bool atomic = p.atom_g != nullptr;  // reduction ablation
-    float *pg = atomic ? p.atom_g : p.part + (size_t)blockIdx.x * ldp;
-    float *pb = atomic ? p.atom_b : p.part + ((size_t)p.G + blockIdx.x) * ldp;
-    auto put = [atomic](float *dst, const float4 &v) {
-        if (atomic) {
-            atomicAdd(dst, v.x);
-            atomicAdd(dst + 1, v.y);
-            atomicAdd(dst + 2, v.z);
-            atomicAdd(dst + 3, v.w);
-        } else {
-            *reinterpret_cast<float4 *>(dst) = v;
-        }
-    };
-    if (slots == 1) {
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int v = ts + j * tpr;
-            if (FULL || v < nvec) {
-#pragma unroll
-                for (int e = 0; e < V; e += 4) {
-                    put(pg + (size_t)v * V + e,
-                        make_float4(acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]));
-                    if constexpr (LN)
-                        put(pb + (size_t)v * V + e, make_float4(acc_b[j * V + e], acc_b[j * V + e + 1],
-                                                                acc_b[j * V + e + 2], acc_b[j * V + e + 3]));
-                }
-            }
-        }
-    } else {
-        // several slots: add their accumulators in slot order, in shared memory
-        __syncthreads();  // every slot is done with its ring stages
-        float *comb = reinterpret_cast<float *>(smem + L.ring_off);
-        float *comb_g = comb + (size_t)slot * ldp;
-        float *comb_b = comb + ((size_t)slots + slot) * ldp;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int v = ts + j * tpr;
-            if (FULL || v < nvec) {
-#pragma unroll
-                for (int e = 0; e < V; e += 4) {
-                    *reinterpret_cast<float4 *>(comb_g + (size_t)v * V + e) = make_float4(
-                        acc_g[j * V + e], acc_g[j * V + e + 1], acc_g[j * V + e + 2], acc_g[j * V + e + 3]);
-                    if constexpr (LN)
-                        *reinterpret_cast<float4 *>(comb_b + (size_t)v * V + e) = make_float4(
-                            acc_b[j * V + e], acc_b[j * V + e + 1], acc_b[j * V + e + 2], acc_b[j * V + e + 3]);
-                }
-            }
-        }
-        __syncthreads();
-        for (int c = tid * 4; c < N; c += blockDim.x * 4) {
-            float4 a = *reinterpret_cast<const float4 *>(comb + c);
-            for (int s2 = 1; s2 < slots; ++s2) {
-                const float4 b = *reinterpret_cast<const float4 *>(comb + (size_t)s2 * ldp + c);
-                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-            }
-            put(pg + c, a);
-            if constexpr (LN) {
-                const float *cb = comb + (size_t)slots * ldp;
-                float4 d = *reinterpret_cast<const float4 *>(cb + c);
-                for (int s2 = 1; s2 < slots; ++s2) {
-                    const float4 b = *reinterpret_cast<const float4 *>(cb + (size_t)s2 * ldp + c);
-                    d.x += b.x; d.y += b.y; d.z += b.z; d.w += b.w;
-                }
-                put(pb + c, d);
-            }
-        }
-    }
+    bwd_store_partials<T, LN, NV, FULL>(p, acc_g, acc_b, smem + L.ring_off, slots, slot, ts, tpr, nvec);
 }
 
 template <typename T, bool LN>
