@@ -365,39 +365,37 @@ def time_steps(prob: Problem, steps: int, warmup: int, flush: L2Flush, world: in
 
 
 def time_e2e(prob: Problem, steps: int):
-    """The backward through the public call with pinned host buffers: H2D of
-    dy, x, gamma and the saved statistics, rms_bwd / ln_bwd, D2H of dx and the
-    parameter gradients, all inside the timed region."""
+    """The backward through the public host-buffer call (ln_bwd_host /
+    rms_bwd_host): every step copies dy, x, gamma and the saved statistics
+    from pinned host memory to the device and dx, dgamma (dbeta) back, the
+    copies pipelined with the kernels over row chunks inside the call."""
     s = prob.stream
     w = prob.w
+    gbn = prob.gbn
     # statistics saved by a forward, kept on the host like the other inputs
     with torch.cuda.stream(s):
         prob.fwd()
     torch.cuda.synchronize()
-    h_in = {"dy": prob.host["dy"].pin_memory(), "x": prob.host["x"].pin_memory(),
-            "gamma": prob.host["gamma"].pin_memory(), "rstd": prob.rstd.cpu().pin_memory()}
+    h = {"dy": prob.host["dy"].pin_memory(), "x": prob.host["x"].pin_memory(),
+         "gamma": prob.host["gamma"].pin_memory(), "rstd": prob.rstd.cpu().pin_memory()}
     if w.has_beta:
-        h_in["mean"] = prob.mean.cpu().pin_memory()
-    h_out = {"dx": torch.empty_like(prob.dx, device="cpu").pin_memory(),
-             "dgamma": torch.empty_like(prob.dgamma, device="cpu").pin_memory()}
+        h["mean"] = prob.mean.cpu().pin_memory()
+    out = {"dx": torch.empty_like(prob.host["x"]).pin_memory(),
+           "dgamma": torch.empty(w.N, dtype=torch.float32).pin_memory()}
     if w.has_beta:
-        h_out["dbeta"] = torch.empty_like(prob.dbeta, device="cpu").pin_memory()
-    d_in = {"dy": prob.dy, "x": prob.x, "gamma": prob.gamma, "rstd": prob.rstd}
-    if w.has_beta:
-        d_in["mean"] = prob.mean
-    d_out = {"dx": prob.dx, "dgamma": prob.dgamma}
-    if w.has_beta:
-        d_out["dbeta"] = prob.dbeta
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+        out["dbeta"] = torch.empty(w.N, dtype=torch.float32).pin_memory()
+    ws = torch.empty(gbn.bwd_host_workspace_bytes(w.M, w.N, prob.tdt, w.has_beta, prob.dev), dtype=torch.uint8,
+                     device=prob.dev)
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in out.values())
 
     def one():
-        with torch.cuda.stream(s):
-            for k, t in h_in.items():
-                d_in[k].copy_(t, non_blocking=True)
-            prob.bwd()
-            for k, t in h_out.items():
-                t.copy_(d_out[k], non_blocking=True)
+        if w.has_beta:
+            gbn.ln_bwd_host(h["dy"], h["x"], h["gamma"], h["mean"], h["rstd"], dx=out["dx"], dgamma=out["dgamma"],
+                            dbeta=out["dbeta"], workspace=ws, device=prob.dev, stream=s)
+        else:
+            gbn.rms_bwd_host(h["dy"], h["x"], h["gamma"], h["rstd"], dx=out["dx"], dgamma=out["dgamma"],
+                             workspace=ws, device=prob.dev, stream=s)
 
     for _ in range(3):
         one()
@@ -527,7 +525,8 @@ def run_ours(args):
             "e2e": {"value": round(world * bwd_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 4),
-                    "what": "pinned host -> device inputs, rms_bwd/ln_bwd, device -> pinned host outputs"},
+                    "what": ("rms_bwd_host / ln_bwd_host: pinned host inputs and outputs, copies in, kernels "
+                             "and copies out pipelined over row chunks inside the call")},
             "gpu_launches": 3 * K + 2 * K,
             "clocks": clocks,
             "wall_s_timed_region": round(wall, 3),

@@ -262,6 +262,39 @@ int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G,
                  int *staged);
 
 /*
+ * Backward from HOST buffers ("Norm backward in Triton -- the dγ/dβ
+ * reduction", section "The gradients"; the same results as ln_bwd / rms_bwd
+ * up to the grouping of the dgamma / dbeta partial sums).
+ *   dy, x, dx: [M, N] row-major host memory of `dtype`; gamma [N] host;
+ *   mean (LayerNorm), rstd: [M] float32 host (the forward's statistics);
+ *   dgamma, dbeta (LayerNorm): [N] float32 host outputs.  Page-locked
+ *   (pinned) host memory lets the copies overlap; pageable memory works but
+ *   its copies serialise.  dx may alias dy.
+ *   workspace: DEVICE memory of at least gbn_bwd_host_workspace_bytes(M, N,
+ *   dtype, has_beta) bytes, any alignment: gamma, the statistics, three
+ *   chunk buffers per tensor, the partial rows and the device dgamma / dbeta.
+ * The rows are cut into chunks of about 16 MiB of each input, after a ramp
+ * of 1/8, 1/4 and 1/2 of that which starts the pipeline sooner.  gamma and the
+ * statistics are copied in first; then chunk i's x and dy are copied in on
+ * one internal stream while chunk i-1's backward runs on `stream` and chunk
+ * i-2's dx is copied out on another internal stream;
+ * the internal streams (two per device, created on first use) are ordered
+ * after the work already on `stream`, and `stream` waits for them at the end,
+ * so the results are complete once `stream` is.  dgamma / dbeta: every chunk
+ * writes its partial rows into one block of the workspace and a single
+ * fixed-order column reduce sums them (deterministic).
+ * Errors: argument errors before anything is enqueued; M = 0 writes zeros
+ * into dgamma / dbeta at once; GBN_ECUDA if a CUDA call fails part-way (the
+ * work enqueued until then still runs).
+ */
+size_t gbn_bwd_host_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta);
+int ln_bwd_host(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
+                float *dgamma, float *dbeta, int64_t M, int64_t N, int dtype, void *workspace,
+                size_t workspace_bytes, cudaStream_t stream);
+int rms_bwd_host(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, float *dgamma,
+                 int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Activation backward ("Norm backward in Triton", section "Activation
  * backward -- fuse it into the epilogue"): dx = dy * f'(preact), the
  * derivative recomputed from the saved pre-activation, for

@@ -79,6 +79,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ln_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, opt, _vp]
     L.rms_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _i64, _i64, _int, _vp, _sz, opt, _vp]
     L.gbn_bwd_plan.argtypes = [_i64, _i64, _int, _int, ctypes.POINTER(_int), ctypes.POINTER(_int)]
+    L.gbn_bwd_host_workspace_bytes.argtypes = [_i64, _i64, _int, _int]
+    L.gbn_bwd_host_workspace_bytes.restype = _sz
+    L.ln_bwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
+    L.rms_bwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
     L.silu_bwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
     L.gelu_bwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
     L.gbn_device_error.argtypes = [_int]
@@ -86,7 +90,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.gbn_status_string.restype = ctypes.c_char_p
     for name in ("ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd", "ln_fwd_ex", "rms_fwd_ex", "ln_bwd_ex", "rms_bwd_ex",
                  "ln_bwd_rows", "rms_bwd_rows",
-                 "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error", "silu_bwd", "gelu_bwd"):
+                 "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error", "silu_bwd", "gelu_bwd",
+                 "ln_bwd_host", "rms_bwd_host"):
         getattr(L, name).restype = _int
     return L
 
@@ -376,3 +381,78 @@ def silu_bwd(dy: torch.Tensor, preact: torch.Tensor, *, dx: Optional[torch.Tenso
 def gelu_bwd(dy: torch.Tensor, preact: torch.Tensor, *, dx: Optional[torch.Tensor] = None, stream=None):
     """dx = dy * GELU'(preact) (exact erf form), elementwise; ``dx`` may be ``dy``."""
     return _act_bwd("gelu_bwd", dy, preact, dx, stream)
+
+
+# ---------------------------------------------------------------------------
+# backward from host buffers (copies pipelined with the kernels)
+# ---------------------------------------------------------------------------
+def bwd_host_workspace_bytes(M: int, N: int, dtype: torch.dtype, has_beta: bool, device=None) -> int:
+    """Device workspace bytes ``ln_bwd_host`` / ``rms_bwd_host`` need."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(lib().gbn_bwd_host_workspace_bytes(M, N, DTYPE_CODES[dtype], int(has_beta)))
+
+
+def _host_args(fn, dy, x, gamma, stats, dx, grads):
+    for name, t in (("dy", dy), ("x", x), ("gamma", gamma)) + stats:
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{fn}: {name} must be a contiguous CPU tensor")
+    if x.dim() != 2 or dy.shape != x.shape or dy.dtype != x.dtype or gamma.dtype != x.dtype:
+        raise ValueError(f"{fn}: dy and x must be [M, N] of one dtype, gamma of that dtype")
+    M, N = x.shape
+    if gamma.numel() != N:
+        raise ValueError(f"{fn}: gamma must have N elements")
+    for name, t in stats:
+        if t.dtype != torch.float32 or t.numel() != M:
+            raise ValueError(f"{fn}: {name} must be float32 with M elements")
+    if dx is None:
+        dx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    elif dx.device.type != "cpu" or not dx.is_contiguous() or dx.shape != x.shape or dx.dtype != x.dtype:
+        raise ValueError(f"{fn}: dx must be a contiguous CPU tensor like x")
+    out = []
+    for name, g in grads:
+        if g is None:
+            g = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        elif g.device.type != "cpu" or g.dtype != torch.float32 or g.numel() != N or not g.is_contiguous():
+            raise ValueError(f"{fn}: {name} must be a contiguous float32 CPU tensor of N elements")
+        out.append(g)
+    return M, N, dx, out
+
+
+def _host_workspace(workspace, M, N, dtype, ln, device):
+    need = bwd_host_workspace_bytes(M, N, dtype, ln, device)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    if workspace.device != torch.device(device) or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a device buffer of at least {need} bytes")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def ln_bwd_host(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor, *,
+                dx=None, dgamma=None, dbeta=None, workspace=None, device=None, stream=None):
+    """LayerNorm backward with every tensor in host memory (pinned for
+    overlap).  Returns (dx, dgamma, dbeta) as CPU tensors, complete once
+    ``stream`` is."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    M, N, dx, (dgamma, dbeta) = _host_args("ln_bwd_host", dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx,
+                                           (("dgamma", dgamma), ("dbeta", dbeta)))
+    workspace, wsb = _host_workspace(workspace, M, N, x.dtype, True, device)
+    with torch.cuda.device(device):
+        _check("ln_bwd_host", lib().ln_bwd_host(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                                _ptr(dgamma), _ptr(dbeta), M, N, _code(x), _ptr(workspace), wsb,
+                                                _stream(device, stream)))
+    return dx, dgamma, dbeta
+
+
+def rms_bwd_host(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: torch.Tensor, *,
+                 dx=None, dgamma=None, workspace=None, device=None, stream=None):
+    """RMSNorm backward with every tensor in host memory (pinned for
+    overlap).  Returns (dx, dgamma) as CPU tensors, complete once ``stream``
+    is."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    M, N, dx, (dgamma,) = _host_args("rms_bwd_host", dy, x, gamma, (("rstd", rstd),), dx, (("dgamma", dgamma),))
+    workspace, wsb = _host_workspace(workspace, M, N, x.dtype, False, device)
+    with torch.cuda.device(device):
+        _check("rms_bwd_host", lib().rms_bwd_host(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
+                                                  _ptr(dgamma), M, N, _code(x), _ptr(workspace), wsb,
+                                                  _stream(device, stream)))
+    return dx, dgamma

@@ -54,7 +54,7 @@ __device__ __forceinline__ void bwd_store_partials(const BwdParams &p, const flo
     const int ldp = p.ldp;
     const bool atomic = p.atom_g != nullptr;  // reduction ablation
     float *pg = atomic ? p.atom_g : p.part + (size_t)blockIdx.x * ldp;
-    float *pb = atomic ? p.atom_b : p.part + ((size_t)p.G + blockIdx.x) * ldp;
+    float *pb = atomic ? p.atom_b : (p.part_b ? p.part_b : p.part + (size_t)p.G * ldp) + (size_t)blockIdx.x * ldp;
     auto put = [atomic](float *dst, const float4 &v) {
         if (atomic) {
             atomicAdd(dst, v.x);
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kGenericThreads) bwd_plain_kernel(const BwdPar
     int nrows;
     block_rows(p.M, p.G, blockIdx.x, row0, nrows);
     float *pg = p.part + (size_t)blockIdx.x * p.ldp;
-    float *pb = p.part + ((size_t)p.G + blockIdx.x) * p.ldp;
+    float *pb = (p.part_b ? p.part_b : p.part + (size_t)p.G * p.ldp) + (size_t)blockIdx.x * p.ldp;
     griddep_launch_dependents();
     // column j is always handled by thread j % blockDim.x: a fixed order per column
     for (int j = threadIdx.x; j < N; j += blockDim.x) {

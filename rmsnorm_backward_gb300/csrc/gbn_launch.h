@@ -46,6 +46,7 @@ struct BwdParams {
     const float *rstd;  // nullptr: no saved statistics, recomputed from x with eps
     void *dx;
     float *part;        // [G][ldp] dgamma partials, then [G][ldp] dbeta partials (LayerNorm)
+    float *part_b;      // non-null: the [G][ldp] dbeta partials start here instead
     int64_t M;
     int N;
     int ldp;            // row stride of the partials, in floats (multiple of 4)

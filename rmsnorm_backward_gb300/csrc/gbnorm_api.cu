@@ -6,6 +6,8 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstring>
+#include <mutex>
 #include <cstdlib>
 
 #include "gbn_launch.h"
@@ -220,19 +222,22 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
 int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
                   void *dx, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes_given,
                   const Opts &o, cudaStream_t stream, float recompute_eps = -1.f, float *dgamma = nullptr,
-                  float *dbeta = nullptr) {
+                  float *dbeta = nullptr, float *part_g = nullptr, float *part_b = nullptr) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (M == 0) return GBN_OK;
     const bool recompute = recompute_eps >= 0.f;
-    if (!dy || !x || !gamma || !dx || !workspace) return GBN_EINVAL;
+    // part_g given (the host-buffer pipeline): the partial rows go there and
+    // to part_b, not into a workspace
+    if (!dy || !x || !gamma || !dx || (!workspace && !part_g)) return GBN_EINVAL;
     if (recompute ? (rstd || mean) : (!rstd || (ln && !mean))) return GBN_EINVAL;
     DevInfo d;
     if ((st = device_info(&d)) != GBN_OK) return st;
-    if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
+    if (!part_g && workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
     BwdParams p{};
     p.dy = dy; p.x = x; p.gamma = gamma; p.mean = mean; p.rstd = rstd; p.dx = dx;
-    p.part = workspace_partials(workspace);
+    p.part = part_g ? part_g : workspace_partials(workspace);
+    p.part_b = part_b;
     p.M = M; p.N = static_cast<int>(N); p.ldp = partial_ld(N); p.G = grid_rows(M, d); p.err = d.err;
     p.l2_hint = env_int("GBN_L2_HINT") != 0;
     p.ld_x = o.ld_x; p.ld_dy = o.ld_dy; p.ld_dx = o.ld_out;
@@ -276,6 +281,183 @@ int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, 
     return cuda_status(launch_colsum(workspace_partials(const_cast<void *>(workspace)), G, partial_ld(N),
                                      static_cast<int>(N), dgamma, ln ? dbeta : nullptr, o.grad_dtype,
                                      o.accumulate, stream));
+}
+
+// ---------------------------------------------------------------------------
+// Backward from host buffers: the rows are cut into chunks of R rows, about
+// kHostChunkBytes per input (each copy costs a few microseconds besides its
+// bytes, so chunks are large), after a ramp of R/8, R/4, R/2 rows that
+// starts the pipeline sooner; chunk i's x and dy are copied in on one
+// internal stream while chunk i-1's backward kernel runs on the caller's
+// stream and chunk i-2's dx is copied out on another, through kHostBufs
+// device buffers per tensor (three: two leave the copies no slack).  gamma
+// and all the statistics are copied in once, first.  Every chunk writes its
+// partial rows at its own offset of one [sum of the chunks' G, ldp] block,
+// and one column reduce over the block (fixed order) gives dgamma / dbeta,
+// copied out last.
+// ---------------------------------------------------------------------------
+constexpr size_t kHostChunkBytes = size_t(16) << 20;
+constexpr int kHostBufs = 3;
+
+struct HostPlan {
+    int64_t R = 0, nchunks = 0, Gtot = 0;
+    size_t gam, st, x[kHostBufs], dy[kHostBufs], dx[kHostBufs], grad, part, total;
+};
+
+// rows of chunk i: R0 * 2^i, capped at R (the ramp), the last chunk what is left
+int64_t host_chunk_rows(int64_t R, int64_t i) {
+    const int64_t r0 = R / 8 > 0 ? R / 8 : 1;
+    return i >= 4 || (r0 << i) >= R ? R : r0 << i;
+}
+
+HostPlan host_plan(int64_t M, int64_t N, int dtype, bool ln, const DevInfo &d) {
+    HostPlan h;
+    const size_t rowb = (size_t)N * elem_bytes(dtype);
+    int64_t R = (int64_t)(kHostChunkBytes / rowb);
+    const int forced = env_int("GBN_HOST_CHUNK_ROWS");
+    if (forced > 0) R = forced;
+    if (R < 1) R = 1;
+    if (R > M) R = M;
+    h.R = R;
+    for (int64_t r0 = 0; r0 < M; ++h.nchunks) {
+        const int64_t want = host_chunk_rows(R, h.nchunks);
+        const int64_t rows = M - r0 < want ? M - r0 : want;
+        h.Gtot += grid_rows(rows, d);
+        r0 += rows;
+    }
+    const int nst = ln ? 2 : 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, 256);
+        return at;
+    };
+    h.gam = take((size_t)N * elem_bytes(dtype));
+    h.st = take((size_t)M * 4 * nst);  // rstd [M], then mean [M]
+    for (int b = 0; b < kHostBufs; ++b) {
+        h.x[b] = take((size_t)R * rowb);
+        h.dy[b] = take((size_t)R * rowb);
+        h.dx[b] = take((size_t)R * rowb);
+    }
+    h.grad = take((size_t)N * 4 * nst);
+    h.part = take((size_t)h.Gtot * partial_ld(N) * 4 * nst);
+    h.total = off + 256;  // the base is aligned up to 256 bytes inside the buffer
+    return h;
+}
+
+// two internal streams per device (copies in, copies out), created on first use
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+};
+HostStreams g_host_streams[kMaxDevices];
+std::mutex g_host_streams_mu;
+
+int host_streams(HostStreams *hs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GBN_ECUDA;
+    std::lock_guard<std::mutex> lock(g_host_streams_mu);
+    HostStreams &h = g_host_streams[dev];
+    if (!h.in) {
+        cudaStream_t a = nullptr, b = nullptr;
+        if (cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking) != cudaSuccess) {
+            if (a) cudaStreamDestroy(a);
+            cudaGetLastError();
+            return GBN_ECUDA;
+        }
+        h.in = a;
+        h.out = b;
+    }
+    *hs = h;
+    return GBN_OK;
+}
+
+int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
+                  void *dx, float *dgamma, float *dbeta, int64_t M, int64_t N, int dtype, void *workspace,
+                  size_t workspace_bytes_given, cudaStream_t s) {
+    int st = check_shape(M, N, dtype);
+    if (st != GBN_OK) return st;
+    if (!dgamma || (ln && !dbeta)) return GBN_EINVAL;
+    if (M == 0) {  // nothing is enqueued: the host outputs are written now
+        memset(dgamma, 0, (size_t)N * 4);
+        if (ln) memset(dbeta, 0, (size_t)N * 4);
+        return GBN_OK;
+    }
+    if (!dy || !x || !gamma || !rstd || (ln && !mean) || !dx || !workspace) return GBN_EINVAL;
+    DevInfo d;
+    if ((st = device_info(&d)) != GBN_OK) return st;
+    const HostPlan h = host_plan(M, N, dtype, ln, d);
+    if (workspace_bytes_given < h.total) return GBN_EWORKSPACE;
+    HostStreams hs;
+    if ((st = host_streams(&hs)) != GBN_OK) return st;
+    unsigned char *base = reinterpret_cast<unsigned char *>(workspace_partials(workspace));
+    const size_t es = elem_bytes(dtype), rowb = (size_t)N * es;
+    const int ldp = partial_ld(N);
+    float *grad = reinterpret_cast<float *>(base + h.grad);
+    float *part = reinterpret_cast<float *>(base + h.part);
+
+    constexpr int B = kHostBufs;
+    cudaEvent_t ev[2 + 3 * B] = {};
+    for (auto &e : ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            for (auto &f : ev)
+                if (f) cudaEventDestroy(f);
+            cudaGetLastError();
+            return GBN_ECUDA;
+        }
+    cudaEvent_t start = ev[0], dx_out = ev[1];
+    cudaEvent_t *loaded = ev + 2, *computed = ev + 2 + B, *unloaded = ev + 2 + 2 * B;
+    const auto chk = [](cudaError_t e) { return e == cudaSuccess; };
+    float *st_r = reinterpret_cast<float *>(base + h.st);
+    float *st_m = st_r + M;
+    bool ok = chk(cudaEventRecord(start, s)) && chk(cudaStreamWaitEvent(hs.in, start, 0)) &&
+              chk(cudaStreamWaitEvent(hs.out, start, 0)) &&
+              chk(cudaMemcpyAsync(base + h.gam, gamma, rowb, cudaMemcpyHostToDevice, hs.in)) &&
+              chk(cudaMemcpyAsync(st_r, rstd, (size_t)M * 4, cudaMemcpyHostToDevice, hs.in)) &&
+              (!ln || chk(cudaMemcpyAsync(st_m, mean, (size_t)M * 4, cudaMemcpyHostToDevice, hs.in)));
+    Opts o;
+    o.ld_x = o.ld_dy = o.ld_out = N;
+    int64_t goff = 0, r0 = 0;
+    for (int64_t i = 0; ok && i < h.nchunks; r0 += host_chunk_rows(h.R, i), ++i) {
+        const int b = static_cast<int>(i % B);
+        const int64_t want = host_chunk_rows(h.R, i), rows = M - r0 < want ? M - r0 : want;
+        // in: the buffers are free once chunk i-B's kernel has read them
+        ok = (i < B || chk(cudaStreamWaitEvent(hs.in, computed[b], 0))) &&
+             chk(cudaMemcpyAsync(base + h.x[b], static_cast<const unsigned char *>(x) + r0 * rowb, rows * rowb,
+                                 cudaMemcpyHostToDevice, hs.in)) &&
+             chk(cudaMemcpyAsync(base + h.dy[b], static_cast<const unsigned char *>(dy) + r0 * rowb, rows * rowb,
+                                 cudaMemcpyHostToDevice, hs.in)) &&
+             chk(cudaEventRecord(loaded[b], hs.in));
+        // compute: dx's buffer is free once chunk i-B's dx has been copied out
+        ok = ok && chk(cudaStreamWaitEvent(s, loaded[b], 0)) &&
+             (i < B || chk(cudaStreamWaitEvent(s, unloaded[b], 0)));
+        if (ok) {
+            const int G = grid_rows(rows, d);
+            st = bwd_rows_impl(ln, base + h.dy[b], base + h.x[b], base + h.gam, ln ? st_m + r0 : nullptr, st_r + r0,
+                               base + h.dx[b], rows, N, dtype, nullptr, 0, o, s, -1.f, nullptr, nullptr,
+                               part + (size_t)goff * ldp, ln ? part + (size_t)(h.Gtot + goff) * ldp : nullptr);
+            goff += G;
+            ok = st == GBN_OK && chk(cudaEventRecord(computed[b], s));
+        }
+        // out
+        ok = ok && chk(cudaStreamWaitEvent(hs.out, computed[b], 0)) &&
+             chk(cudaMemcpyAsync(static_cast<unsigned char *>(dx) + r0 * rowb, base + h.dx[b], rows * rowb,
+                                 cudaMemcpyDeviceToHost, hs.out)) &&
+             chk(cudaEventRecord(unloaded[b], hs.out));
+    }
+    if (ok) {
+        ok = chk(launch_colsum(part, static_cast<int>(h.Gtot), ldp, static_cast<int>(N), grad,
+                               ln ? grad + N : nullptr, GBN_F32, false, s)) &&
+             chk(cudaMemcpyAsync(dgamma, grad, (size_t)N * 4, cudaMemcpyDeviceToHost, s)) &&
+             (!ln || chk(cudaMemcpyAsync(dbeta, grad + N, (size_t)N * 4, cudaMemcpyDeviceToHost, s))) &&
+             chk(cudaEventRecord(dx_out, hs.out)) && chk(cudaStreamWaitEvent(s, dx_out, 0));
+    }
+    for (auto &e : ev) cudaEventDestroy(e);  // released once the work recorded on them is done
+    if (!ok) {
+        cudaGetLastError();
+        return st != GBN_OK ? st : GBN_ECUDA;
+    }
+    return GBN_OK;
 }
 
 }  // namespace
@@ -415,6 +597,26 @@ int silu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype,
 
 int gelu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype, cudaStream_t stream) {
     return act_bwd_impl(kActGelu, dy, preact, dx, n, dtype, stream);
+}
+
+size_t gbn_bwd_host_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta) {
+    if (check_shape(M, N, dtype) != GBN_OK || M <= 0) return 0;
+    DevInfo d;
+    if (device_info(&d) != GBN_OK) return 0;
+    return host_plan(M, N, dtype, has_beta != 0, d).total;
+}
+
+int ln_bwd_host(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
+                float *dgamma, float *dbeta, int64_t M, int64_t N, int dtype, void *workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
+    return bwd_host_impl(true, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, M, N, dtype, workspace,
+                         workspace_bytes, stream);
+}
+
+int rms_bwd_host(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, float *dgamma,
+                 int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return bwd_host_impl(false, dy, x, gamma, nullptr, rstd, dx, dgamma, nullptr, M, N, dtype, workspace,
+                         workspace_bytes, stream);
 }
 
 int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *staged) {

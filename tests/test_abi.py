@@ -75,3 +75,15 @@ def test_activation_host_checks(lib):
         assert fn(p, p, None, 8, 2, None) == 1
         assert fn(p, p, p, -1, 2, None) == 1      # negative size
         assert fn(p, p, p, 8, 5, None) == 2       # unknown dtype
+
+
+def test_host_buffer_entry_checks(lib):
+    import rmsnorm_backward_gb300 as gbn
+    L = gbn._declare(ctypes.CDLL(gbn.library_path))
+    p = ctypes.c_void_p(16)
+    assert L.rms_bwd_host(None, p, p, p, p, p, 4, 8, 2, p, 1 << 20, None) == 1     # null input
+    assert L.rms_bwd_host(p, p, p, p, p, None, 4, 8, 2, p, 1 << 20, None) == 1     # null dgamma
+    assert L.rms_bwd_host(p, p, p, p, p, p, 4, 8, 7, p, 1 << 20, None) == 2        # dtype
+    assert L.rms_bwd_host(p, p, p, p, p, p, -1, 8, 2, p, 1 << 20, None) == 1       # M < 0
+    assert L.ln_bwd_host(p, p, p, None, p, p, p, p, 4, 8, 2, p, 1 << 20, None) == 1  # LayerNorm without mean
+    assert L.ln_bwd_host(p, p, p, p, p, p, p, None, 4, 8, 2, p, 1 << 20, None) == 1  # LayerNorm without dbeta
