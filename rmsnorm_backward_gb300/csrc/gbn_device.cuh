@@ -125,6 +125,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// one arrival (release semantics: this thread's earlier writes are visible
+// to a thread that then observes the phase complete)
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -141,6 +147,27 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
+}
+
+// a counter in shared memory written by one thread and polled by others
+__device__ __forceinline__ void st_release_shared(int *p, int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
+// Waits until *counter > k, giving up after ~limit_ns.  Returns false on giving up.
+__device__ __forceinline__ bool wait_counter_above(const int *counter, int k, uint64_t limit_ns = 2000000000ull) {
+    if (ld_acquire_shared(counter) > k) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < (1u << 28); ++it) {
+        if (ld_acquire_shared(counter) > k) return true;
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
 }
 
 // Waits for the phase of `bar` with the given parity to complete, giving up

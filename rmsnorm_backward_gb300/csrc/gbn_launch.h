@@ -121,6 +121,8 @@ cudaError_t launch_fwd_plain(int dtype, bool ln, const FwdParams &p, cudaStream_
 cudaError_t launch_bwd_staged(int dtype, bool ln, int nv, bool full, const BwdParams &p, size_t smem,
                               cudaStream_t s);
 cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_t s);
+// warp-specialised backward (bwd_ws.cuh): vo vectors per output lane
+cudaError_t launch_bwd_ws(int dtype, bool ln, int vo, const BwdParams &p, int threads, size_t smem, cudaStream_t s);
 // dgamma / dbeta from the partial rows; out_dtype is GBN_F32 or the storage
 // dtype of the parameters (rounded to nearest even); accumulate adds the
 // buffers' previous contents (widened) to the sums before the store

@@ -10,6 +10,7 @@
 #include <mutex>
 #include <cstdlib>
 
+#include "bwd_ws_layout.h"
 #include "gbn_launch.h"
 #include "gbnorm.h"
 
@@ -248,13 +249,36 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     }
     const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma) &&
                          stride16(o.ld_x, dtype) && stride16(o.ld_dy, dtype) && stride16(o.ld_out, dtype);
-    StagedPlan P;
-    if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
-    if (P.ok) {
-        p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
-        st = cuda_status(launch_bwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
-    } else {
-        st = cuda_status(launch_bwd_plain(dtype, ln, p, stream));
+    // the warp-specialised kernel: saved statistics, rows of whole warps of
+    // vectors, >= 2 stages (every reduce mode, so dx does not depend on it)
+    int ws_no = 0, ws_vo = 0;
+    bool launched = false;
+    if (aligned && !recompute && env_int("GBN_NO_WS") == 0 &&
+        N % (16 / elem_bytes(dtype)) == 0 && ws_shape(static_cast<int>(N / (16 / elem_bytes(dtype))), &ws_no, &ws_vo) &&
+        ws_no == 16) {  // measured faster there: shorter rows leave too few output warps, and
+                        // at 4 vectors a lane (ws_shape refuses it) the slot kernel was faster
+        const size_t rowb = (size_t)N * elem_bytes(dtype);
+        const int stat_rows = static_cast<int>((M + p.G - 1) / p.G);
+        for (int S = 16; S >= 2; --S) {
+            const WsLayout W = ws_layout(ln, rowb, S, stat_rows);
+            if (W.total <= static_cast<size_t>(d.smem_optin)) {
+                p.stages = S;
+                p.stat_rows = stat_rows;
+                st = cuda_status(launch_bwd_ws(dtype, ln, ws_vo, p, 32 * (1 + kSumWarps + ws_no), W.total, stream));
+                launched = true;
+                break;
+            }
+        }
+    }
+    if (!launched) {
+        StagedPlan P;
+        if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
+        if (P.ok) {
+            p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
+            st = cuda_status(launch_bwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
+        } else {
+            st = cuda_status(launch_bwd_plain(dtype, ln, p, stream));
+        }
     }
     if (st == GBN_OK && o.reduce_mode == GBN_REDUCE_COLWALK)
         st = cuda_status(launch_colwalk(dtype, ln, p, dgamma, ln ? dbeta : nullptr, o.accumulate, stream));
