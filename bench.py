@@ -105,8 +105,8 @@ def measured_hbm_peak():
 
 # the sources each captured kernel is built from
 KERNEL_SOURCES = {
-    "bwd_staged_kernel": ("gbn_device.cuh", "gbn_launch.h", "bwd_kernels.cuh", "bwd_f32.cu", "bwd_f16.cu",
-                          "bwd_bf16.cu"),
+    "bwd_staged_kernel": ("gbn_device.cuh", "gbn_launch.h", "bwd_kernels.cuh"),
+    "bwd_ws_kernel": ("gbn_device.cuh", "gbn_launch.h", "bwd_ws_layout.h", "bwd_ws.cuh"),
     "act_bwd_kernel": ("gbn_device.cuh", "gbn_launch.h", "act_bwd.cu"),
 }
 
@@ -123,13 +123,13 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of a workload's dominant kernel from an ncu
-    capture, if the capture was taken of that kernel's current sources."""
+    capture, if the capture was taken of that kernel and its current sources."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f).get(workload)
-        if not rec or rec.get("source_hash") != kernel_source_hash(rec["kernel"]):
+        if not rec or rec.get("kernel") != kernel or rec.get("source_hash") != kernel_source_hash(kernel):
             return None
     except Exception:
         return None
@@ -453,7 +453,8 @@ def run_ours(args):
     flush = L2Flush(device)
     import rmsnorm_backward_gb300 as gbn
 
-    G, staged = gbn.bwd_plan(w.M, w.N, prob.tdt, w.has_beta, device)
+    G, kind = gbn.bwd_plan(w.M, w.N, prob.tdt, w.has_beta, device)
+    kernel = gbn.BWD_KERNELS[kind]
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
     with ClockSampler(gpu_index, enabled=not args.no_clocks) as clk:
@@ -499,7 +500,7 @@ def run_ours(args):
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "l2": ("flushed before the forward and before the backward of every step: a 256 MiB write, "
                        "then a 256 MiB read of another buffer so no dirty lines carry into the timed kernel"),
-                "G": G, "staged_kernel": staged, "stats": args.stats, "reduce": args.reduce,
+                "G": G, "bwd_kernel": kernel, "stats": args.stats, "reduce": args.reduce,
                 "step": "forward (y, stats) then backward (dx + partial rows, then column reduce)",
                 "timed": ("value = backward minimum bytes / device time of the public backward call (rows kernel "
                           "+ column reduce, CUDA events around the call); roofline = rows kernel alone, own loop"),
@@ -516,8 +517,8 @@ def run_ours(args):
             "bwd_min_bytes": bwd_bytes,
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": ("bwd_staged_kernel (dx + per-CTA partial rows)"
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name, kernel),
+                "kernel": (f"{kernel} (dx + per-CTA partial rows)"
                            if args.stats == "saved" and args.reduce == "partials" else
                            "the whole backward call (ablation / save-nothing variant)"),
                 "algorithmic_bytes_per_launch": rows_bytes, "peak_source": peak_src,
@@ -696,7 +697,7 @@ def run_activation(args):
             "us": round(avg * 1e6, 3),
             "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "roofline": {"bound": "hbm", "achieved": round(nbytes / avg / 1e9, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(nbytes / avg / 1e9 / peak, 4), "traffic": recorded_traffic(a.name),
+                         "frac": round(nbytes / avg / 1e9 / peak, 4), "traffic": recorded_traffic(a.name, "act_bwd_kernel"),
                          "kernel": "act_bwd_kernel", "algorithmic_bytes_per_launch": nbytes,
                          "peak_source": peak_src},
             "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",

@@ -254,9 +254,10 @@ int gbn_bwd_reduce(const void *workspace, size_t workspace_bytes, int64_t M,
 /*
  * Describes the launch the backward takes for an [M, N] problem on the
  * current device: *G = number of row blocks (CTAs, rows of the partial
- * workspace), *staged = 1 if 16-byte aligned buffers take the bulk-copy
- * staged kernel (0 = plain-load kernel for every alignment).  Either output
- * pointer may be NULL.  Returns a gbn_status.
+ * workspace), and for 16-byte aligned buffers and saved statistics
+ * *staged = 2 (the warp-specialised bulk-copy kernel), 1 (the slot-staged
+ * bulk-copy kernel) or 0 (the plain-load kernel, which every alignment can
+ * take).  Either output pointer may be NULL.  Returns a gbn_status.
  */
 int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G,
                  int *staged);

@@ -176,13 +176,18 @@ def bwd_workspace_bytes(M: int, N: int, dtype: torch.dtype, has_beta: bool, devi
         return int(lib().gbn_bwd_workspace_bytes(M, N, DTYPE_CODES[dtype], int(has_beta)))
 
 
-def bwd_plan(M: int, N: int, dtype: torch.dtype, has_beta: bool, device=None) -> Tuple[int, bool]:
-    """(G, staged): the number of row blocks and whether aligned buffers take the staged kernel."""
+BWD_KERNELS = {0: "bwd_plain_kernel", 1: "bwd_staged_kernel", 2: "bwd_ws_kernel"}
+
+
+def bwd_plan(M: int, N: int, dtype: torch.dtype, has_beta: bool, device=None) -> Tuple[int, int]:
+    """(G, kind): the number of row blocks and the kernel aligned buffers with
+    saved statistics take: 2 warp-specialised, 1 slot-staged, 0 plain
+    (names in BWD_KERNELS)."""
     G, staged = _int(0), _int(0)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _check("gbn_bwd_plan", lib().gbn_bwd_plan(M, N, DTYPE_CODES[dtype], int(has_beta),
                                                   ctypes.byref(G), ctypes.byref(staged)))
-    return G.value, bool(staged.value)
+    return G.value, int(staged.value)
 
 
 def device_error(clear: bool = True, device=None) -> int:

@@ -218,6 +218,39 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
     return cuda_status(launch_fwd_plain(dtype, ln, p, stream));
 }
 
+// The warp-specialised backward's launch (saved statistics, aligned buffers):
+// rows of 16 output warps x 32 lanes x 1-2 vectors, where it measured faster
+// (shorter rows leave too few output warps; at 4 vectors a lane, which
+// ws_shape refuses, the slot kernel was faster), and >= 2 stages.
+struct WsPlan {
+    bool ok = false;
+    int vo = 0, threads = 0, stages = 0, stat_rows = 0;
+    size_t smem = 0;
+};
+
+WsPlan ws_plan(bool ln, int dtype, int64_t M, int64_t N, int G, const DevInfo &d) {
+    WsPlan w;
+    const int V = 16 / elem_bytes(dtype);
+    int no = 0, vo = 0;
+    if (env_int("GBN_NO_WS") != 0 || N % V != 0 || !ws_shape(static_cast<int>(N / V), &no, &vo) || no != 16)
+        return w;
+    const size_t rowb = (size_t)N * elem_bytes(dtype);
+    const int stat_rows = static_cast<int>((M + G - 1) / G);
+    for (int S = 16; S >= 2; --S) {
+        const WsLayout L = ws_layout(ln, rowb, S, stat_rows);
+        if (L.total <= static_cast<size_t>(d.smem_optin)) {
+            w.ok = true;
+            w.vo = vo;
+            w.threads = 32 * (1 + kSumWarps + no);
+            w.stages = S;
+            w.stat_rows = stat_rows;
+            w.smem = L.total;
+            break;
+        }
+    }
+    return w;
+}
+
 // recompute_eps >= 0: no saved statistics (mean / rstd null), the kernels
 // form them from x with this eps; < 0: the statistics are required.
 int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
@@ -249,25 +282,15 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     }
     const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(gamma) &&
                          stride16(o.ld_x, dtype) && stride16(o.ld_dy, dtype) && stride16(o.ld_out, dtype);
-    // the warp-specialised kernel: saved statistics, rows of whole warps of
-    // vectors, >= 2 stages (every reduce mode, so dx does not depend on it)
-    int ws_no = 0, ws_vo = 0;
+    // the warp-specialised kernel (every reduce mode, so dx does not depend on it)
     bool launched = false;
-    if (aligned && !recompute && env_int("GBN_NO_WS") == 0 &&
-        N % (16 / elem_bytes(dtype)) == 0 && ws_shape(static_cast<int>(N / (16 / elem_bytes(dtype))), &ws_no, &ws_vo) &&
-        ws_no == 16) {  // measured faster there: shorter rows leave too few output warps, and
-                        // at 4 vectors a lane (ws_shape refuses it) the slot kernel was faster
-        const size_t rowb = (size_t)N * elem_bytes(dtype);
-        const int stat_rows = static_cast<int>((M + p.G - 1) / p.G);
-        for (int S = 16; S >= 2; --S) {
-            const WsLayout W = ws_layout(ln, rowb, S, stat_rows);
-            if (W.total <= static_cast<size_t>(d.smem_optin)) {
-                p.stages = S;
-                p.stat_rows = stat_rows;
-                st = cuda_status(launch_bwd_ws(dtype, ln, ws_vo, p, 32 * (1 + kSumWarps + ws_no), W.total, stream));
-                launched = true;
-                break;
-            }
+    if (aligned && !recompute) {
+        const WsPlan w = ws_plan(ln, dtype, M, N, p.G, d);
+        if (w.ok) {
+            p.stages = w.stages;
+            p.stat_rows = w.stat_rows;
+            st = cuda_status(launch_bwd_ws(dtype, ln, w.vo, p, w.threads, w.smem, stream));
+            launched = true;
         }
     }
     if (!launched) {
@@ -650,7 +673,13 @@ int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *sta
     if ((st = device_info(&d)) != GBN_OK) return st;
     const int g = grid_rows(M, d);
     if (G) *G = g;
-    if (staged) *staged = M > 0 && staged_plan(true, has_beta != 0, dtype, M, N, g, d).ok ? 1 : 0;
+    if (staged) {
+        *staged = 0;
+        if (M > 0 && ws_plan(has_beta != 0, dtype, M, N, g, d).ok)
+            *staged = 2;
+        else if (M > 0 && staged_plan(true, has_beta != 0, dtype, M, N, g, d).ok)
+            *staged = 1;
+    }
     return GBN_OK;
 }
 
