@@ -365,20 +365,30 @@ namespace gbn {
 // ---------------------------------------------------------------------------
 // dgamma / dbeta column sums of the [G][ldp] partial rows, in one fixed order
 // ---------------------------------------------------------------------------
-constexpr int kColsumSlices = 16;
-constexpr int kColsumBatch = 8;  // loads a thread issues together (16 measured no faster)
+// Two shapes: 8 slices (256-thread CTAs) beside the warp-specialised rows
+// kernel, where they fit beside it on an SM and so start, as its
+// programmatic dependent, as soon as that grid completes (16 slices measured
+// 1.2-1.6 us slower there, 4 slices slower too); 16 slices (512 threads)
+// beside the other rows kernels, which leave no room for them (8 slices
+// measured up to 2 us slower there).
+template <int SLICES>
+struct ColsumShape {
+    static constexpr int kBatch = 192 / SLICES;  // loads a thread issues together: one batch up to G = 192
+};
 
 // sum over g < G of P[g*ldp + c], for c in [c0, c1), 32 columns a
-// pass: lane q of slice s (threads 32*s + q, s < 16) adds rows s, s+16, ...
-// in increasing order (eight loads issued together), then slice 0 adds the
-// 16 slice sums in slice order.  Every CTA shape that calls this gives the
-// same bits per column.  Needs at least 512 threads (the others only join
-// the barriers) and sm[16][33].  P is read through L2 (written by an
-// earlier grid).
+// pass: lane q of slice s (threads 32*s + q, s < SLICES) adds rows s,
+// s + SLICES, ... in increasing order (ColsumShape::kBatch loads issued
+// together), then slice 0 adds the slice sums in slice order.  Every CTA
+// shape with the same SLICES gives the same bits per column.  Needs at
+// least 32 * SLICES threads (the others only join the barriers) and
+// sm[SLICES][33].  P is read through L2 (written by an earlier grid).
 // store(c, sum) writes the result of column c.
-template <typename Store>
+template <int SLICES, typename Store>
 __device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int c0, int c1, Store store,
                                              float (*sm)[33]) {
+    constexpr int kColsumSlices = SLICES;
+    constexpr int kColsumBatch = ColsumShape<SLICES>::kBatch;
     const int q = threadIdx.x & 31, slice = threadIdx.x >> 5;
     for (int cb = c0; cb < c1; cb += 32) {
         const int c = cb + q;

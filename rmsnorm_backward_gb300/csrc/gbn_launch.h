@@ -127,7 +127,7 @@ cudaError_t launch_bwd_ws(int dtype, bool ln, int vo, const BwdParams &p, int th
 // dtype of the parameters (rounded to nearest even); accumulate adds the
 // buffers' previous contents (widened) to the sums before the store
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
-                          bool accumulate, cudaStream_t s);
+                          bool accumulate, bool small, cudaStream_t s);
 
 // reduction ablation: dgamma (dbeta) = sum over rows of dy*xhat (dy), each CTA
 // owning 32 columns and walking every row of x and dy in order

@@ -256,7 +256,7 @@ WsPlan ws_plan(bool ln, int dtype, int64_t M, int64_t N, int G, const DevInfo &d
 int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
                   void *dx, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes_given,
                   const Opts &o, cudaStream_t stream, float recompute_eps = -1.f, float *dgamma = nullptr,
-                  float *dbeta = nullptr, float *part_g = nullptr, float *part_b = nullptr) {
+                  float *dbeta = nullptr, float *part_g = nullptr, float *part_b = nullptr, int *kind = nullptr) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (M == 0) return GBN_OK;
@@ -291,6 +291,7 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
             p.stat_rows = w.stat_rows;
             st = cuda_status(launch_bwd_ws(dtype, ln, w.vo, p, w.threads, w.smem, stream));
             launched = true;
+            if (kind) *kind = 2;
         }
     }
     if (!launched) {
@@ -299,8 +300,10 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
         if (P.ok) {
             p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
             st = cuda_status(launch_bwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
+            if (kind) *kind = 1;
         } else {
             st = cuda_status(launch_bwd_plain(dtype, ln, p, stream));
+            if (kind) *kind = 0;
         }
     }
     if (st == GBN_OK && o.reduce_mode == GBN_REDUCE_COLWALK)
@@ -308,8 +311,12 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     return st;
 }
 
+// rows_kind: the kernel that wrote the partial rows (2 warp-specialised, 1
+// slot, 0 plain), or -1 when unknown (the phase call), then taken from the
+// shape as the saved-statistics backward would choose it.  It picks the
+// reduce's CTA shape: small CTAs beside the warp-specialised kernel.
 int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, int64_t N, int dtype, bool ln,
-                void *dgamma, void *dbeta, const Opts &o, cudaStream_t stream) {
+                void *dgamma, void *dbeta, const Opts &o, cudaStream_t stream, int rows_kind = -1) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (!dgamma || (ln && !dbeta)) return GBN_EINVAL;
@@ -325,9 +332,10 @@ int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, 
     if ((st = device_info(&d)) != GBN_OK) return st;
     if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
     const int G = grid_rows(M, d);
+    const bool small = rows_kind >= 0 ? rows_kind == 2 : ws_plan(ln, dtype, M, N, G, d).ok;
     return cuda_status(launch_colsum(workspace_partials(const_cast<void *>(workspace)), G, partial_ld(N),
                                      static_cast<int>(N), dgamma, ln ? dbeta : nullptr, o.grad_dtype,
-                                     o.accumulate, stream));
+                                     o.accumulate, small, stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -465,6 +473,7 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     Opts o;
     o.ld_x = o.ld_dy = o.ld_out = N;
     int64_t goff = 0, r0 = 0;
+    int last_kind = 0;
     for (int64_t i = 0; ok && i < h.nchunks; r0 += host_chunk_rows(h.R, i), ++i) {
         const int b = static_cast<int>(i % B);
         const int64_t want = host_chunk_rows(h.R, i), rows = M - r0 < want ? M - r0 : want;
@@ -482,7 +491,8 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
             const int G = grid_rows(rows, d);
             st = bwd_rows_impl(ln, base + h.dy[b], base + h.x[b], base + h.gam, ln ? st_m + r0 : nullptr, st_r + r0,
                                base + h.dx[b], rows, N, dtype, nullptr, 0, o, s, -1.f, nullptr, nullptr,
-                               part + (size_t)goff * ldp, ln ? part + (size_t)(h.Gtot + goff) * ldp : nullptr);
+                               part + (size_t)goff * ldp, ln ? part + (size_t)(h.Gtot + goff) * ldp : nullptr,
+                               &last_kind);
             goff += G;
             ok = st == GBN_OK && chk(cudaEventRecord(computed[b], s));
         }
@@ -494,7 +504,7 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     }
     if (ok) {
         ok = chk(launch_colsum(part, static_cast<int>(h.Gtot), ldp, static_cast<int>(N), grad,
-                               ln ? grad + N : nullptr, GBN_F32, false, s)) &&
+                               ln ? grad + N : nullptr, GBN_F32, false, last_kind == 2, s)) &&
              chk(cudaMemcpyAsync(dgamma, grad, (size_t)N * 4, cudaMemcpyDeviceToHost, s)) &&
              (!ln || chk(cudaMemcpyAsync(dbeta, grad + N, (size_t)N * 4, cudaMemcpyDeviceToHost, s))) &&
              chk(cudaEventRecord(dx_out, hs.out)) && chk(cudaStreamWaitEvent(s, dx_out, 0));
@@ -586,10 +596,12 @@ int ln_bwd_ex(const void *dy, const void *x, const void *gamma, const float *mea
         if (st == GBN_OK) st = cuda_status(cudaMemsetAsync(dbeta, 0, (size_t)N * 4, stream));
         if (st != GBN_OK) return st;
     }
+    int kind = 0;
     st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
-                       recompute ? eps : -1.f, static_cast<float *>(dgamma), static_cast<float *>(dbeta));
+                       recompute ? eps : -1.f, static_cast<float *>(dgamma), static_cast<float *>(dbeta), nullptr,
+                       nullptr, &kind);
     if (st != GBN_OK || (M > 0 && o.reduce_mode != GBN_REDUCE_PARTIALS)) return st;
-    return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, o, stream);
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, o, stream, kind);
 }
 
 int rms_bwd_ex(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, void *dgamma,
@@ -608,10 +620,11 @@ int rms_bwd_ex(const void *dy, const void *x, const void *gamma, const float *rs
         st = cuda_status(cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream));
         if (st != GBN_OK) return st;
     }
+    int kind = 0;
     st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
-                       recompute ? eps : -1.f, static_cast<float *>(dgamma), nullptr);
+                       recompute ? eps : -1.f, static_cast<float *>(dgamma), nullptr, nullptr, nullptr, &kind);
     if (st != GBN_OK || (M > 0 && o.reduce_mode != GBN_REDUCE_PARTIALS)) return st;
-    return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, o, stream);
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, o, stream, kind);
 }
 
 int ln_bwd(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,

@@ -17,19 +17,20 @@ namespace gbn {
 static __device__ int g_error_flag = 0;
 
 // dgamma (blockIdx.y = 0) or dbeta (blockIdx.y = 1): CTA x sums columns
-// [32x, 32x + 32) of the partial rows with colsum_range (one fixed order).
-template <typename OutT, bool ACC>
-__global__ void __launch_bounds__(32 * kColsumSlices) colsum_kernel(const float *__restrict__ part, int G, int ldp,
+// [32x, 32x + 32) of the partial rows with colsum_range (one fixed order per
+// SLICES).
+template <typename OutT, bool ACC, int SLICES>
+__global__ void __launch_bounds__(32 * SLICES) colsum_kernel(const float *__restrict__ part, int G, int ldp,
                                                                      int N, OutT *__restrict__ dgamma,
                                                                      OutT *__restrict__ dbeta) {
-    __shared__ float sm[kColsumSlices][33];
+    __shared__ float sm[SLICES][33];
     griddep_wait();  // the partial rows of the kernel before this one
     const float *P = part + (size_t)blockIdx.y * G * ldp;
     OutT *out = blockIdx.y ? dbeta : dgamma;
     const int c0 = blockIdx.x * 32;
     // accumulate: the buffer's previous value is added after the fixed-order
     // sum; 16-bit outputs are rounded to nearest even
-    colsum_range(
+    colsum_range<SLICES>(
         P, G, ldp, c0, min(N, c0 + 32),
         [&](int c, float t) {
             if constexpr (std::is_same<OutT, float>::value) {
@@ -122,11 +123,11 @@ cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_
     return cudaErrorInvalidValue;
 }
 
-template <typename OutT, bool ACC>
+template <typename OutT, bool ACC, int SLICES>
 cudaError_t launch_colsum_t(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + 31) / 32, dbeta ? 2 : 1);
-    cfg.blockDim = dim3(32 * kColsumSlices);
+    cfg.blockDim = dim3(32 * SLICES);
     cfg.stream = s;
     // launched as a programmatic dependent of the rows kernel before it
     cudaLaunchAttribute attr[1];
@@ -134,23 +135,26 @@ cudaError_t launch_colsum_t(const float *part, int G, int ldp, int N, void *dgam
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, colsum_kernel<OutT, ACC>, part, G, ldp, N, static_cast<OutT *>(dgamma),
+    return cudaLaunchKernelEx(&cfg, colsum_kernel<OutT, ACC, SLICES>, part, G, ldp, N, static_cast<OutT *>(dgamma),
                               static_cast<OutT *>(dbeta));
 }
 
 template <typename OutT>
-cudaError_t launch_colsum_acc(const float *part, int G, int ldp, int N, void *dg, void *db, bool acc,
+cudaError_t launch_colsum_acc(const float *part, int G, int ldp, int N, void *dg, void *db, bool acc, bool small,
                               cudaStream_t s) {
-    return acc ? launch_colsum_t<OutT, true>(part, G, ldp, N, dg, db, s)
-               : launch_colsum_t<OutT, false>(part, G, ldp, N, dg, db, s);
+    if (small)
+        return acc ? launch_colsum_t<OutT, true, 8>(part, G, ldp, N, dg, db, s)
+                   : launch_colsum_t<OutT, false, 8>(part, G, ldp, N, dg, db, s);
+    return acc ? launch_colsum_t<OutT, true, 16>(part, G, ldp, N, dg, db, s)
+               : launch_colsum_t<OutT, false, 16>(part, G, ldp, N, dg, db, s);
 }
 
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
-                          bool accumulate, cudaStream_t s) {
+                          bool accumulate, bool small, cudaStream_t s) {
     switch (out_dtype) {
-        case 0: return launch_colsum_acc<float>(part, G, ldp, N, dgamma, dbeta, accumulate, s);
-        case 1: return launch_colsum_acc<__half>(part, G, ldp, N, dgamma, dbeta, accumulate, s);
-        case 2: return launch_colsum_acc<__nv_bfloat16>(part, G, ldp, N, dgamma, dbeta, accumulate, s);
+        case 0: return launch_colsum_acc<float>(part, G, ldp, N, dgamma, dbeta, accumulate, small, s);
+        case 1: return launch_colsum_acc<__half>(part, G, ldp, N, dgamma, dbeta, accumulate, small, s);
+        case 2: return launch_colsum_acc<__nv_bfloat16>(part, G, ldp, N, dgamma, dbeta, accumulate, small, s);
     }
     return cudaErrorInvalidValue;
 }
