@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(32 * (1 + kSumWarps + 16), 1) bwd_ws_kernel(co
                 }
                 const int64_t row = row0 + issued;
                 unsigned char *dst = ring + (size_t)pos.stage * 2 * rowb;
+                // the consumers' shared loads of the stage (seen through
+                // `consumed`) come before the copy that overwrites it
+                if (issued >= S) fence_proxy_async();
                 mbar_arrive_expect_tx(&full[pos.stage], static_cast<uint32_t>(2 * rowb));
                 bulk_load_nohint(dst, static_cast<const T *>(p.x) + row * p.ld_x, static_cast<uint32_t>(rowb),
                                  &full[pos.stage]);
