@@ -23,7 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "norm_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libnorm_oracle.so")
-GCC_FLAGS = ["-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11"]
+GCC_FLAGS = ["-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11", "-pthread"]
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -68,6 +68,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_rms_bwd.argtypes = [_I, _I, _P, _P, _P, _P, _P, _P]
     for f in ("oracle_silu_bwd", "oracle_gelu_bwd", "oracle_silu_fwd", "oracle_gelu_fwd"):
         getattr(lib, f).argtypes = [_I, _P, _P, _P][: 4 if f.endswith("bwd") else 3]
+    lib.oracle_ln_bwd_threads.argtypes = [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int]
+    lib.oracle_rms_bwd_threads.argtypes = [_I, _I, _P, _P, _P, _P, _P, _P, ctypes.c_int]
+    lib.oracle_ln_bwd_threads.restype = ctypes.c_int
+    lib.oracle_rms_bwd_threads.restype = ctypes.c_int
     for f in ("oracle_ln_fwd", "oracle_rms_fwd", "oracle_ln_bwd", "oracle_rms_bwd", "oracle_silu_bwd",
               "oracle_gelu_bwd", "oracle_silu_fwd", "oracle_gelu_fwd"):
         getattr(lib, f).restype = None
@@ -111,23 +115,37 @@ def rms_fwd(x, gamma, eps: float, lib: Optional[ctypes.CDLL] = None):
     return y, rstd
 
 
-def ln_bwd(dy, x, gamma, mean, rstd, lib: Optional[ctypes.CDLL] = None):
-    """LayerNorm backward from saved stats. Returns (dx [M,N], dgamma [N], dbeta [N])."""
+def ln_bwd(dy, x, gamma, mean, rstd, lib: Optional[ctypes.CDLL] = None, threads: int = 1):
+    """LayerNorm backward from saved stats. Returns (dx [M,N], dgamma [N], dbeta [N]).
+
+    threads > 1: the timed mode across host threads (row blocks, partial
+    sums added in thread order), for the CPU baseline."""
     lib = lib or load()
     dy, x, gamma, mean, rstd = _d(dy), _d(x), _d(gamma), _d(mean).reshape(-1), _d(rstd).reshape(-1)
     M, N = _shape(x)
     dx = np.empty((M, N)); dg = np.empty(N); db = np.empty(N)
-    lib.oracle_ln_bwd(M, N, _p(dy), _p(x), _p(gamma), _p(mean), _p(rstd), _p(dx), _p(dg), _p(db))
+    if threads > 1:
+        if lib.oracle_ln_bwd_threads(M, N, _p(dy), _p(x), _p(gamma), _p(mean), _p(rstd), _p(dx), _p(dg), _p(db),
+                                     threads) != 0:
+            raise RuntimeError("oracle_ln_bwd_threads failed")
+    else:
+        lib.oracle_ln_bwd(M, N, _p(dy), _p(x), _p(gamma), _p(mean), _p(rstd), _p(dx), _p(dg), _p(db))
     return dx, dg, db
 
 
-def rms_bwd(dy, x, gamma, rstd, lib: Optional[ctypes.CDLL] = None):
-    """RMSNorm backward from the saved rstd. Returns (dx [M,N], dgamma [N])."""
+def rms_bwd(dy, x, gamma, rstd, lib: Optional[ctypes.CDLL] = None, threads: int = 1):
+    """RMSNorm backward from the saved rstd. Returns (dx [M,N], dgamma [N]).
+
+    threads > 1: the timed mode across host threads, as for ln_bwd."""
     lib = lib or load()
     dy, x, gamma, rstd = _d(dy), _d(x), _d(gamma), _d(rstd).reshape(-1)
     M, N = _shape(x)
     dx = np.empty((M, N)); dg = np.empty(N)
-    lib.oracle_rms_bwd(M, N, _p(dy), _p(x), _p(gamma), _p(rstd), _p(dx), _p(dg))
+    if threads > 1:
+        if lib.oracle_rms_bwd_threads(M, N, _p(dy), _p(x), _p(gamma), _p(rstd), _p(dx), _p(dg), threads) != 0:
+            raise RuntimeError("oracle_rms_bwd_threads failed")
+    else:
+        lib.oracle_rms_bwd(M, N, _p(dy), _p(x), _p(gamma), _p(rstd), _p(dx), _p(dg))
     return dx, dg
 
 

@@ -36,7 +36,9 @@
  * x86-64 and aarch64 hosts give identical results).
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 /* LayerNorm forward, [NB] "The gradients" (forward line) and [LN5] ln_fwd. */
 void oracle_ln_fwd(int64_t M, int64_t N, const double *x, const double *gamma,
@@ -197,4 +199,94 @@ void oracle_gelu_fwd(int64_t n, const double *x, double *y)
     const double inv_sqrt2 = 0.70710678118654752440;
     for (int64_t i = 0; i < n; ++i)
         y[i] = x[i] * 0.5 * erfc(-x[i] * inv_sqrt2);
+}
+
+/*
+ * Timed mode across host threads, for the CPU baseline only: the rows are
+ * split into nthreads contiguous blocks, each thread runs the functions
+ * above on its block with its own dgamma / dbeta partial, and the partials
+ * are added in thread order.  dx is identical to the single-thread call;
+ * dgamma / dbeta differ only in the grouping of the row sums.  Returns 0, or
+ * -1 if a thread or a partial buffer could not be created.
+ */
+struct oracle_block {
+    int ln;
+    int64_t rows, N;
+    const double *dy, *x, *gamma, *mean, *rstd;
+    double *dx, *dgamma, *dbeta;
+};
+
+static void *oracle_block_run(void *arg)
+{
+    struct oracle_block *b = (struct oracle_block *)arg;
+    if (b->ln)
+        oracle_ln_bwd(b->rows, b->N, b->dy, b->x, b->gamma, b->mean, b->rstd, b->dx, b->dgamma, b->dbeta);
+    else
+        oracle_rms_bwd(b->rows, b->N, b->dy, b->x, b->gamma, b->rstd, b->dx, b->dgamma);
+    return 0;
+}
+
+static int oracle_bwd_threads(int ln, int64_t M, int64_t N, const double *dy, const double *x,
+                              const double *gamma, const double *mean, const double *rstd, double *dx,
+                              double *dgamma, double *dbeta, int nthreads)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > M)
+        nthreads = M > 0 ? (int)M : 1;
+    struct oracle_block *blk = calloc((size_t)nthreads, sizeof *blk);
+    pthread_t *tid = calloc((size_t)nthreads, sizeof *tid);
+    double *part = calloc((size_t)nthreads * (size_t)N * 2, sizeof(double));
+    int rc = (blk && tid && part) ? 0 : -1;
+    int started = 0;
+    for (int t = 0; rc == 0 && t < nthreads; ++t) {
+        const int64_t r0 = M * t / nthreads, r1 = M * (t + 1) / nthreads;
+        struct oracle_block *b = &blk[t];
+        b->ln = ln;
+        b->rows = r1 - r0;
+        b->N = N;
+        b->dy = dy + r0 * N;
+        b->x = x + r0 * N;
+        b->gamma = gamma;
+        b->mean = ln ? mean + r0 : 0;
+        b->rstd = rstd + r0;
+        b->dx = dx + r0 * N;
+        b->dgamma = part + (size_t)t * N * 2;
+        b->dbeta = b->dgamma + N;
+        if (pthread_create(&tid[t], 0, oracle_block_run, b) != 0)
+            rc = -1;
+        else
+            ++started;
+    }
+    for (int t = 0; t < started; ++t)
+        pthread_join(tid[t], 0);
+    if (rc == 0) {
+        for (int64_t j = 0; j < N; ++j) {
+            double g = 0.0, be = 0.0;
+            for (int t = 0; t < nthreads; ++t) {
+                g += part[(size_t)t * N * 2 + j];
+                be += part[(size_t)t * N * 2 + N + j];
+            }
+            dgamma[j] = g;
+            if (ln)
+                dbeta[j] = be;
+        }
+    }
+    free(part);
+    free(tid);
+    free(blk);
+    return rc;
+}
+
+int oracle_ln_bwd_threads(int64_t M, int64_t N, const double *dy, const double *x, const double *gamma,
+                          const double *mean, const double *rstd, double *dx, double *dgamma, double *dbeta,
+                          int nthreads)
+{
+    return oracle_bwd_threads(1, M, N, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, nthreads);
+}
+
+int oracle_rms_bwd_threads(int64_t M, int64_t N, const double *dy, const double *x, const double *gamma,
+                           const double *rstd, double *dx, double *dgamma, int nthreads)
+{
+    return oracle_bwd_threads(0, M, N, dy, x, gamma, 0, rstd, dx, dgamma, 0, nthreads);
 }
