@@ -24,7 +24,8 @@ import torch
 
 __all__ = [
     "GbnError", "GbnOptions", "lib", "library_path", "ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd",
-    "ln_bwd_rows", "rms_bwd_rows", "bwd_reduce", "bwd_workspace_bytes", "bwd_plan",
+    "ln_bwd_rows", "rms_bwd_rows", "bwd_reduce", "bwd_workspace_bytes", "bwd_plan", "BWD_KERNELS",
+    "ln_bwd_host", "rms_bwd_host", "bwd_host_workspace_bytes", "silu_bwd", "gelu_bwd", "REDUCE_MODES",
     "device_error", "status_string", "DTYPE_CODES",
 ]
 
