@@ -309,6 +309,25 @@ int silu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype,
 int gelu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype, cudaStream_t stream);
 
 /*
+ * The activation backward from HOST buffers: dy, preact (in), dx (out) are n
+ * elements of `dtype` in host memory (pinned for overlap; dx may alias dy).
+ * workspace: DEVICE memory of at least gbn_act_host_workspace_bytes(n,
+ * dtype) bytes, any alignment.  The elements are cut into chunks of about
+ * 16 MiB of each tensor (after a ramp of 1/8, 1/4, 1/2 of that); chunk i is
+ * copied in on an internal stream while chunk i-1's kernel runs on `stream`
+ * and chunk i-2's dx is copied out on another internal stream, through
+ * three device buffers per tensor; `stream` waits for the internal streams
+ * at the end, so dx is complete once `stream` is.  Errors as for silu_bwd,
+ * plus GBN_EWORKSPACE; GBN_ECUDA if a CUDA call fails part-way (the work
+ * enqueued until then still runs).
+ */
+size_t gbn_act_host_workspace_bytes(int64_t n, int dtype);
+int silu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
+int gelu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Every wait inside the library's kernels (on a shared-memory barrier that
  * a bulk copy completes) gives up after about two seconds; the kernel then
  * records an error code in a per-device flag, drains its own copies with

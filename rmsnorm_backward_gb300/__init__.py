@@ -26,6 +26,7 @@ __all__ = [
     "GbnError", "GbnOptions", "lib", "library_path", "ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd",
     "ln_bwd_rows", "rms_bwd_rows", "bwd_reduce", "bwd_workspace_bytes", "bwd_plan", "BWD_KERNELS",
     "ln_bwd_host", "rms_bwd_host", "bwd_host_workspace_bytes", "silu_bwd", "gelu_bwd", "REDUCE_MODES",
+    "silu_bwd_host", "gelu_bwd_host",
     "device_error", "status_string", "DTYPE_CODES",
 ]
 
@@ -84,6 +85,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.gbn_bwd_host_workspace_bytes.restype = _sz
     L.ln_bwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
     L.rms_bwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
+    L.gbn_act_host_workspace_bytes.argtypes = [_i64, _int]
+    L.gbn_act_host_workspace_bytes.restype = _sz
+    L.silu_bwd_host.argtypes = [_vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]
+    L.gelu_bwd_host.argtypes = [_vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]
     L.silu_bwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
     L.gelu_bwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
     L.gbn_device_error.argtypes = [_int]
@@ -92,7 +97,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd", "ln_fwd_ex", "rms_fwd_ex", "ln_bwd_ex", "rms_bwd_ex",
                  "ln_bwd_rows", "rms_bwd_rows",
                  "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error", "silu_bwd", "gelu_bwd",
-                 "ln_bwd_host", "rms_bwd_host"):
+                 "ln_bwd_host", "rms_bwd_host", "silu_bwd_host", "gelu_bwd_host"):
         getattr(L, name).restype = _int
     return L
 
@@ -462,3 +467,38 @@ def rms_bwd_host(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: t
                                                   _ptr(dgamma), M, N, _code(x), _ptr(workspace), wsb,
                                                   _stream(device, stream)))
     return dx, dgamma
+
+
+def _act_host(fn: str, dy: torch.Tensor, preact: torch.Tensor, dx, workspace, device, stream):
+    for name, t in (("dy", dy), ("preact", preact)):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{fn}: {name} must be a contiguous CPU tensor")
+    if dy.shape != preact.shape or dy.dtype != preact.dtype:
+        raise ValueError(f"{fn}: dy and preact must match in shape and dtype")
+    code = _code(dy)
+    if dx is None:
+        dx = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True)
+    elif dx.device.type != "cpu" or not dx.is_contiguous() or dx.shape != dy.shape or dx.dtype != dy.dtype:
+        raise ValueError(f"{fn}: dx must be a contiguous CPU tensor like dy")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        need = int(lib().gbn_act_host_workspace_bytes(dy.numel(), code))
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+        wsb = workspace.numel() * workspace.element_size()
+        if workspace.device != device or wsb < need:
+            raise ValueError(f"{fn}: workspace must be a device buffer of at least {need} bytes")
+        _check(fn, getattr(lib(), fn)(_ptr(dy), _ptr(preact), _ptr(dx), dy.numel(), code, _ptr(workspace), wsb,
+                                      _stream(device, stream)))
+    return dx
+
+
+def silu_bwd_host(dy: torch.Tensor, preact: torch.Tensor, *, dx=None, workspace=None, device=None, stream=None):
+    """silu_bwd with dy, preact and dx in host memory (pinned for overlap);
+    dx is complete once ``stream`` is."""
+    return _act_host("silu_bwd_host", dy, preact, dx, workspace, device, stream)
+
+
+def gelu_bwd_host(dy: torch.Tensor, preact: torch.Tensor, *, dx=None, workspace=None, device=None, stream=None):
+    """gelu_bwd with dy, preact and dx in host memory (pinned for overlap)."""
+    return _act_host("gelu_bwd_host", dy, preact, dx, workspace, device, stream)

@@ -517,6 +517,96 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     return GBN_OK;
 }
 
+// Activation backward from host buffers: the same pipeline as the norm's
+// (copies in on one internal stream, the kernel on the caller's stream,
+// copies out on the other, three device buffers per tensor), over chunks of
+// elements: about kHostChunkBytes of each tensor after the same ramp.
+struct ActHostPlan {
+    int64_t R = 0, nchunks = 0;
+    size_t dy[kHostBufs], pre[kHostBufs], dx[kHostBufs], total = 0;
+};
+
+ActHostPlan act_host_plan(int64_t n, int dtype) {
+    ActHostPlan h;
+    const size_t es = elem_bytes(dtype);
+    int64_t R = (int64_t)(kHostChunkBytes / es);
+    const int forced = env_int("GBN_HOST_CHUNK_ROWS");  // elements here
+    if (forced > 0) R = forced;
+    if (R > n) R = n;
+    if (R < 1) R = 1;
+    h.R = R;
+    for (int64_t e0 = 0; e0 < n; ++h.nchunks) e0 += host_chunk_rows(R, h.nchunks);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, 256);
+        return at;
+    };
+    for (int b = 0; b < kHostBufs; ++b) {
+        h.dy[b] = take((size_t)R * es);
+        h.pre[b] = take((size_t)R * es);
+        h.dx[b] = take((size_t)R * es);
+    }
+    h.total = off + 256;
+    return h;
+}
+
+int act_host_impl(int act, const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                  size_t workspace_bytes_given, cudaStream_t s) {
+    if (!valid_dtype(dtype)) return GBN_EDTYPE;
+    if (n < 0) return GBN_EINVAL;
+    if (n == 0) return GBN_OK;
+    if (!dy || !preact || !dx || !workspace) return GBN_EINVAL;
+    DevInfo d;
+    int st = device_info(&d);
+    if (st != GBN_OK) return st;
+    const ActHostPlan h = act_host_plan(n, dtype);
+    if (workspace_bytes_given < h.total) return GBN_EWORKSPACE;
+    HostStreams hs;
+    if ((st = host_streams(&hs)) != GBN_OK) return st;
+    unsigned char *base = reinterpret_cast<unsigned char *>(workspace_partials(workspace));
+    const size_t es = elem_bytes(dtype);
+    constexpr int B = kHostBufs;
+    cudaEvent_t ev[2 + 3 * B] = {};
+    for (auto &e : ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            for (auto &f : ev)
+                if (f) cudaEventDestroy(f);
+            cudaGetLastError();
+            return GBN_ECUDA;
+        }
+    cudaEvent_t start = ev[0], out_done = ev[1];
+    cudaEvent_t *loaded = ev + 2, *computed = ev + 2 + B, *unloaded = ev + 2 + 2 * B;
+    const auto chk = [](cudaError_t e) { return e == cudaSuccess; };
+    bool ok = chk(cudaEventRecord(start, s)) && chk(cudaStreamWaitEvent(hs.in, start, 0)) &&
+              chk(cudaStreamWaitEvent(hs.out, start, 0));
+    int64_t e0 = 0;
+    for (int64_t i = 0; ok && i < h.nchunks; e0 += host_chunk_rows(h.R, i), ++i) {
+        const int b = static_cast<int>(i % B);
+        const int64_t want = host_chunk_rows(h.R, i), cnt = n - e0 < want ? n - e0 : want;
+        const size_t off = (size_t)e0 * es, bytes = (size_t)cnt * es;
+        ok = (i < B || chk(cudaStreamWaitEvent(hs.in, computed[b], 0))) &&
+             chk(cudaMemcpyAsync(base + h.dy[b], static_cast<const unsigned char *>(dy) + off, bytes,
+                                 cudaMemcpyHostToDevice, hs.in)) &&
+             chk(cudaMemcpyAsync(base + h.pre[b], static_cast<const unsigned char *>(preact) + off, bytes,
+                                 cudaMemcpyHostToDevice, hs.in)) &&
+             chk(cudaEventRecord(loaded[b], hs.in)) && chk(cudaStreamWaitEvent(s, loaded[b], 0)) &&
+             (i < B || chk(cudaStreamWaitEvent(s, unloaded[b], 0))) &&
+             chk(launch_act_bwd(act, dtype, base + h.dy[b], base + h.pre[b], base + h.dx[b], cnt, d.sms, d.err, s)) &&
+             chk(cudaEventRecord(computed[b], s)) && chk(cudaStreamWaitEvent(hs.out, computed[b], 0)) &&
+             chk(cudaMemcpyAsync(static_cast<unsigned char *>(dx) + off, base + h.dx[b], bytes,
+                                 cudaMemcpyDeviceToHost, hs.out)) &&
+             chk(cudaEventRecord(unloaded[b], hs.out));
+    }
+    ok = ok && chk(cudaEventRecord(out_done, hs.out)) && chk(cudaStreamWaitEvent(s, out_done, 0));
+    for (auto &e : ev) cudaEventDestroy(e);  // released once the work recorded on them is done
+    if (!ok) {
+        cudaGetLastError();
+        return GBN_ECUDA;
+    }
+    return GBN_OK;
+}
+
 }  // namespace
 }  // namespace gbn
 
@@ -677,6 +767,21 @@ int rms_bwd_host(const void *dy, const void *x, const void *gamma, const float *
                  int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     return bwd_host_impl(false, dy, x, gamma, nullptr, rstd, dx, dgamma, nullptr, M, N, dtype, workspace,
                          workspace_bytes, stream);
+}
+
+size_t gbn_act_host_workspace_bytes(int64_t n, int dtype) {
+    if (!valid_dtype(dtype) || n <= 0) return 0;
+    return act_host_plan(n, dtype).total;
+}
+
+int silu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+    return act_host_impl(kActSilu, dy, preact, dx, n, dtype, workspace, workspace_bytes, stream);
+}
+
+int gelu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+    return act_host_impl(kActGelu, dy, preact, dx, n, dtype, workspace, workspace_bytes, stream);
 }
 
 int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *staged) {

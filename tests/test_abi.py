@@ -87,3 +87,15 @@ def test_host_buffer_entry_checks(lib):
     assert L.rms_bwd_host(p, p, p, p, p, p, -1, 8, 2, p, 1 << 20, None) == 1       # M < 0
     assert L.ln_bwd_host(p, p, p, None, p, p, p, p, 4, 8, 2, p, 1 << 20, None) == 1  # LayerNorm without mean
     assert L.ln_bwd_host(p, p, p, p, p, p, p, None, 4, 8, 2, p, 1 << 20, None) == 1  # LayerNorm without dbeta
+
+
+def test_activation_host_entry_checks(lib):
+    import rmsnorm_backward_gb300 as gbn
+    L = gbn._declare(ctypes.CDLL(gbn.library_path))
+    p = ctypes.c_void_p(16)
+    for fn in (L.silu_bwd_host, L.gelu_bwd_host):
+        assert fn(p, p, p, 0, 2, p, 1 << 20, None) == 0      # empty: no-op
+        assert fn(None, p, p, 8, 2, p, 1 << 20, None) == 1   # null input
+        assert fn(p, p, p, 8, 2, None, 1 << 20, None) == 1   # no workspace
+        assert fn(p, p, p, -1, 2, p, 1 << 20, None) == 1     # negative size
+        assert fn(p, p, p, 8, 9, p, 1 << 20, None) == 2      # unknown dtype
