@@ -457,6 +457,8 @@ def run_ours(args):
     import rmsnorm_backward_gb300 as gbn
 
     G, kind = gbn.bwd_plan(w.M, w.N, prob.tdt, w.has_beta, device)
+    if args.stats == "recompute" and kind == 2:
+        kind = 1  # without saved statistics the slot-staged kernel runs
     kernel = gbn.BWD_KERNELS[kind]
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
