@@ -286,7 +286,8 @@ int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G,
  * fixed-order column reduce sums them (deterministic).
  * Errors: argument errors before anything is enqueued; M = 0 writes zeros
  * into dgamma / dbeta at once; GBN_ECUDA if a CUDA call fails part-way (the
- * work enqueued until then still runs).
+ * work enqueued until then still runs, and `stream` is made to wait for it
+ * where CUDA still allows, so the buffers may be reused in stream order).
  */
 size_t gbn_bwd_host_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta);
 int ln_bwd_host(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
@@ -319,7 +320,7 @@ int gelu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype,
  * three device buffers per tensor; `stream` waits for the internal streams
  * at the end, so dx is complete once `stream` is.  Errors as for silu_bwd,
  * plus GBN_EWORKSPACE; GBN_ECUDA if a CUDA call fails part-way (the work
- * enqueued until then still runs).
+ * enqueued until then still runs, and `stream` waits for it as above).
  */
 size_t gbn_act_host_workspace_bytes(int64_t n, int dtype);
 int silu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,

@@ -25,15 +25,22 @@ struct DevInfo {
     int *err = nullptr;
 };
 
-// per-device properties, filled once per device (racing fills write the same values)
+// per-device properties, filled once per device under a lock, then read
+// without one once the ready flag is seen
 DevInfo g_dev[kMaxDevices];
 std::atomic<int> g_dev_ready[kMaxDevices];
+std::mutex g_dev_mu;
 
 int device_info(DevInfo *out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GBN_ECUDA;
     if (dev < 0 || dev >= kMaxDevices) return GBN_ECUDA;
     if (!g_dev_ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (g_dev_ready[dev].load(std::memory_order_relaxed)) {
+            *out = g_dev[dev];
+            return GBN_OK;
+        }
         DevInfo d;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
@@ -407,6 +414,16 @@ struct HostStreams {
 HostStreams g_host_streams[kMaxDevices];
 std::mutex g_host_streams_mu;
 
+// After a failed enqueue part-way through a host-buffer call: the caller's
+// stream still waits for everything the internal streams were given, so the
+// caller may reuse or free its buffers in stream order.  Best effort: errors
+// here are dropped, the call already reports its own.
+void join_internal_streams(const HostStreams &hs, cudaEvent_t e_in, cudaEvent_t e_out, cudaStream_t s) {
+    if (cudaEventRecord(e_in, hs.in) == cudaSuccess) cudaStreamWaitEvent(s, e_in, 0);
+    if (cudaEventRecord(e_out, hs.out) == cudaSuccess) cudaStreamWaitEvent(s, e_out, 0);
+    cudaGetLastError();
+}
+
 int host_streams(HostStreams *hs) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GBN_ECUDA;
@@ -509,6 +526,7 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
              (!ln || chk(cudaMemcpyAsync(dbeta, grad + N, (size_t)N * 4, cudaMemcpyDeviceToHost, s))) &&
              chk(cudaEventRecord(dx_out, hs.out)) && chk(cudaStreamWaitEvent(s, dx_out, 0));
     }
+    if (!ok) join_internal_streams(hs, start, dx_out, s);
     for (auto &e : ev) cudaEventDestroy(e);  // released once the work recorded on them is done
     if (!ok) {
         cudaGetLastError();
@@ -599,6 +617,7 @@ int act_host_impl(int act, const void *dy, const void *preact, void *dx, int64_t
              chk(cudaEventRecord(unloaded[b], hs.out));
     }
     ok = ok && chk(cudaEventRecord(out_done, hs.out)) && chk(cudaStreamWaitEvent(s, out_done, 0));
+    if (!ok) join_internal_streams(hs, start, out_done, s);
     for (auto &e : ev) cudaEventDestroy(e);  // released once the work recorded on them is done
     if (!ok) {
         cudaGetLastError();
