@@ -56,6 +56,8 @@ def parse_args(argv=None):
                     help="cross-row reduction of dgamma/dbeta: the deterministic default or an ablation")
     ap.add_argument("--stats", choices=["saved", "recompute"], default="saved",
                     help="recompute: the backward gets no saved statistics and forms them from x")
+    ap.add_argument("--kernel", choices=["auto", "slot", "plain"], default="auto",
+                    help="the rows kernel of the public backward: the fastest that applies, or a forced one")
     ap.add_argument("--activation", choices=["silu", "gelu"], default=None,
                     help="time the activation backward on a 16384 x 4096 bf16 tensor instead of the norm")
     return ap.parse_args(argv)
@@ -204,7 +206,8 @@ class ClockSampler:
 class Problem:
     """Device buffers and the three launches of one step for a workload."""
 
-    def __init__(self, w: wl.Workload, device, stream, recompute: bool = False, reduce: str = "partials"):
+    def __init__(self, w: wl.Workload, device, stream, recompute: bool = False, reduce: str = "partials",
+                 kernel: str = "auto"):
         import rmsnorm_backward_gb300 as gbn
 
         self.gbn = gbn
@@ -244,21 +247,17 @@ class Problem:
                                     P(self.rstd), w.eps, M, N, code, sp))
             self._rows = (L.ln_bwd_rows, (P(self.dy), P(self.x), P(self.gamma), P(self.mean), P(self.rstd),
                                           P(self.dx), M, N, code, P(self.ws), wsb, sp))
-            self._rows_recompute = (L.ln_bwd_ex, (P(self.dy), P(self.x), P(self.gamma), None, None, P(self.dx),
-                                                  P(self.dgamma), P(self.dbeta), w.eps, M, N, code, P(self.ws), wsb,
-                                                  None, sp))
         else:
             self._fwd = (L.rms_fwd, (P(self.x), P(self.gamma), P(self.y), P(self.rstd), w.eps, M, N, code, sp))
             self._rows = (L.rms_bwd_rows, (P(self.dy), P(self.x), P(self.gamma), P(self.rstd), P(self.dx), M, N,
                                            code, P(self.ws), wsb, sp))
-            self._rows_recompute = (L.rms_bwd_ex, (P(self.dy), P(self.x), P(self.gamma), None, P(self.dx),
-                                                   P(self.dgamma), w.eps, M, N, code, P(self.ws), wsb, None, sp))
         self._red = (L.gbn_bwd_reduce, (P(self.ws), wsb, M, N, code, int(w.has_beta), P(self.dgamma),
                                         P(self.dbeta), sp))
         # the public backward through the options call (contiguous rows,
         # float32 grads, overwrite, the chosen cross-row reduction)
-        self.opt = gbn.GbnOptions(N, N, N, 0, 0, gbn.REDUCE_MODES[reduce])
+        self.opt = gbn.GbnOptions(N, N, N, 0, 0, gbn.REDUCE_MODES[reduce], gbn.KERNELS[kernel], 0, 0)
         self.reduce = reduce
+        self.kernel = kernel
         optp = ctypes.byref(self.opt)
         if w.has_beta:
             self._bwd = (L.ln_bwd_ex, (P(self.dy), P(self.x), P(self.gamma), P(bmean), P(brstd), P(self.dx),
@@ -276,13 +275,17 @@ class Problem:
     def fwd(self):
         self._call(self._fwd)
 
+    def rows_alone(self) -> bool:
+        """Whether the rows kernel can be timed on its own (the phase call):
+        saved statistics, the default reduce and the automatic kernel."""
+        return not self.recompute and self.reduce == "partials" and self.kernel == "auto"
+
     def bwd_rows(self):
-        # the save-nothing backward has no separate rows phase: time the
-        # whole call (rows kernel + reduce) there
-        self._call(self._rows_recompute if self.recompute else (self._bwd if self.reduce != "partials" else self._rows))
+        # otherwise there is no separate rows phase: time the whole call
+        self._call(self._rows if self.rows_alone() else self._bwd)
 
     def bwd_reduce(self):
-        if not self.recompute and self.reduce == "partials":
+        if self.rows_alone():
             self._call(self._red)
 
     def bwd_fused(self):
@@ -452,13 +455,13 @@ def run_ours(args):
     device = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device)
-    prob = Problem(w, device, stream, recompute=args.stats == "recompute", reduce=args.reduce)
+    prob = Problem(w, device, stream, recompute=args.stats == "recompute", reduce=args.reduce, kernel=args.kernel)
     flush = L2Flush(device)
     import rmsnorm_backward_gb300 as gbn
 
     G, kind = gbn.bwd_plan(w.M, w.N, prob.tdt, w.has_beta, device)
-    if args.stats == "recompute" and kind == 2:
-        kind = 1  # without saved statistics the slot-staged kernel runs
+    if args.kernel != "auto":
+        kind = {"slot": 1 if kind else 0, "plain": 0}[args.kernel]
     kernel = gbn.BWD_KERNELS[kind]
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
@@ -505,7 +508,7 @@ def run_ours(args):
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "l2": ("flushed before the forward and before the backward of every step: a 256 MiB write, "
                        "then a 256 MiB read of another buffer so no dirty lines carry into the timed kernel"),
-                "G": G, "bwd_kernel": kernel, "stats": args.stats, "reduce": args.reduce,
+                "G": G, "bwd_kernel": kernel, "stats": args.stats, "reduce": args.reduce, "kernel": args.kernel,
                 "step": "forward (y, stats) then backward (dx + partial rows, then column reduce)",
                 "timed": ("value = backward minimum bytes / device time of the public backward call (rows kernel "
                           "+ column reduce, CUDA events around the call); roofline = rows kernel alone, own loop"),
@@ -523,10 +526,14 @@ def run_ours(args):
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name, kernel),
-                "kernel": (f"{kernel} (dx + per-CTA partial rows)"
-                           if args.stats == "saved" and args.reduce == "partials" else
-                           "the whole backward call (ablation / save-nothing variant)"),
+                "kernel": (f"{kernel} (dx + per-CTA partial rows) alone, against the measured copy rate"
+                           if prob.rows_alone() else
+                           "the whole backward call (ablation, forced kernel or save-nothing variant)"),
                 "algorithmic_bytes_per_launch": rows_bytes, "peak_source": peak_src,
+                # the spec reading: the fused backward (rows kernel +
+                # column reduce) against the nominal 8 TB/s
+                "frac_nominal": round(value / world / NOMINAL_HBM_GBS, 4),
+                "frac_nominal_what": "public backward call (rows kernel + column reduce) GB/s / 8000 GB/s",
             },
             "e2e": {"value": round(world * bwd_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -170,8 +170,27 @@ int rms_bwd(const void *dy, const void *x, const void *gamma, const float *rstd,
  *       kernel ln_bwd_dwdb); deterministic, one more read of x and dy.
  *       Needs grad_dtype GBN_F32 and the saved statistics.
  *     The last two exist to measure what the default costs or saves.
+ *   kernel: which kernel takes the rows (forward and backward).
+ *     GBN_KERNEL_AUTO (0, the default): the fastest one that applies.
+ *     GBN_KERNEL_SLOT (1): the slot-staged bulk-copy kernel, never the
+ *       warp-specialised backward; the plain kernel where rows are not
+ *       16-byte aligned.
+ *     GBN_KERNEL_PLAIN (2): the plain-load kernel.
+ *     Every kernel gives the same results up to float32 rounding order, and
+ *     dgamma / dbeta keep one summation order per (M, N, dtype, device)
+ *     for a given kernel.
+ *   host_chunk (host-buffer calls only): rows (norm) or elements
+ *     (activation) per pipeline chunk; 0 means about 16 MiB of each input.
+ *   wait_limit_ns (backward): how long a kernel's warp waits for data from
+ *     another warp or a bulk copy before it gives up and reports error 1
+ *     through gbn_device_error(); 0 means two seconds.  The wait for the
+ *     kernel's own copies in flight before it exits keeps its own limit.
+ *     A diagnostic: a tiny value makes the waits run out on purpose, so the
+ *     error path can be tested without a fault.
+ * Fields that a call does not use must be zero.
  */
 enum { GBN_REDUCE_PARTIALS = 0, GBN_REDUCE_ATOMIC = 1, GBN_REDUCE_COLWALK = 2 };
+enum { GBN_KERNEL_AUTO = 0, GBN_KERNEL_SLOT = 1, GBN_KERNEL_PLAIN = 2 };
 
 typedef struct {
     int64_t ld_x;
@@ -180,6 +199,9 @@ typedef struct {
     int accumulate;
     int grad_dtype;
     int reduce_mode;
+    int kernel;
+    int64_t host_chunk;
+    int64_t wait_limit_ns;
 } gbn_options;
 
 /* The four operations with gbn_options; dgamma / dbeta are `void *` of type
@@ -297,6 +319,20 @@ int rms_bwd_host(const void *dy, const void *x, const void *gamma, const float *
                  int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * The host-buffer backward with gbn_options.  Of the options, only
+ * host_chunk (rows per chunk after the ramp; 0 = about 16 MiB of each
+ * input), kernel and wait_limit_ns apply; the others must be zero.  The
+ * workspace size depends on host_chunk.
+ */
+size_t gbn_bwd_host_workspace_bytes_ex(int64_t M, int64_t N, int dtype, int has_beta, const gbn_options *opt);
+int ln_bwd_host_ex(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
+                   void *dx, float *dgamma, float *dbeta, int64_t M, int64_t N, int dtype, void *workspace,
+                   size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream);
+int rms_bwd_host_ex(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, float *dgamma,
+                    int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes,
+                    const gbn_options *opt, cudaStream_t stream);
+
+/*
  * Activation backward ("Norm backward in Triton", section "Activation
  * backward -- fuse it into the epilogue"): dx = dy * f'(preact), the
  * derivative recomputed from the saved pre-activation, for
@@ -327,6 +363,15 @@ int silu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int d
                   size_t workspace_bytes, cudaStream_t stream);
 int gelu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream);
+
+/* The host-buffer activation backward with gbn_options: only host_chunk
+ * (elements per chunk after the ramp; 0 = about 16 MiB of each tensor)
+ * applies; the other fields must be zero. */
+size_t gbn_act_host_workspace_bytes_ex(int64_t n, int dtype, const gbn_options *opt);
+int silu_bwd_host_ex(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                     size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream);
+int gelu_bwd_host_ex(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                     size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream);
 
 /*
  * Every wait inside the library's kernels (on a shared-memory barrier that

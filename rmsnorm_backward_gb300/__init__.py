@@ -25,7 +25,7 @@ import torch
 __all__ = [
     "GbnError", "GbnOptions", "lib", "library_path", "ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd",
     "ln_bwd_rows", "rms_bwd_rows", "bwd_reduce", "bwd_workspace_bytes", "bwd_plan", "BWD_KERNELS",
-    "ln_bwd_host", "rms_bwd_host", "bwd_host_workspace_bytes", "silu_bwd", "gelu_bwd", "REDUCE_MODES",
+    "ln_bwd_host", "rms_bwd_host", "bwd_host_workspace_bytes", "silu_bwd", "gelu_bwd", "REDUCE_MODES", "KERNELS",
     "silu_bwd_host", "gelu_bwd_host",
     "device_error", "status_string", "DTYPE_CODES",
 ]
@@ -50,11 +50,15 @@ class GbnOptions(ctypes.Structure):
     """gbn_options of include/gbnorm.h."""
 
     _fields_ = [("ld_x", ctypes.c_int64), ("ld_dy", ctypes.c_int64), ("ld_out", ctypes.c_int64),
-                ("accumulate", ctypes.c_int), ("grad_dtype", ctypes.c_int), ("reduce_mode", ctypes.c_int)]
+                ("accumulate", ctypes.c_int), ("grad_dtype", ctypes.c_int), ("reduce_mode", ctypes.c_int),
+                ("kernel", ctypes.c_int), ("host_chunk", ctypes.c_int64), ("wait_limit_ns", ctypes.c_int64)]
 
 
 # reduce_mode values (GBN_REDUCE_* of include/gbnorm.h)
 REDUCE_MODES = {"partials": 0, "atomic": 1, "colwalk": 2}
+# kernel values (GBN_KERNEL_*): the fastest that applies, the slot-staged
+# kernel (never the warp-specialised backward), the plain-load kernel
+KERNELS = {"auto": 0, "slot": 1, "plain": 2}
 
 
 class GbnError(RuntimeError):
@@ -85,6 +89,14 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.gbn_bwd_host_workspace_bytes.restype = _sz
     L.ln_bwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
     L.rms_bwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]
+    L.gbn_bwd_host_workspace_bytes_ex.argtypes = [_i64, _i64, _int, _int, opt]
+    L.gbn_bwd_host_workspace_bytes_ex.restype = _sz
+    L.ln_bwd_host_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, opt, _vp]
+    L.rms_bwd_host_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp, _sz, opt, _vp]
+    L.gbn_act_host_workspace_bytes_ex.argtypes = [_i64, _int, opt]
+    L.gbn_act_host_workspace_bytes_ex.restype = _sz
+    L.silu_bwd_host_ex.argtypes = [_vp, _vp, _vp, _i64, _int, _vp, _sz, opt, _vp]
+    L.gelu_bwd_host_ex.argtypes = [_vp, _vp, _vp, _i64, _int, _vp, _sz, opt, _vp]
     L.gbn_act_host_workspace_bytes.argtypes = [_i64, _int]
     L.gbn_act_host_workspace_bytes.restype = _sz
     L.silu_bwd_host.argtypes = [_vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]
@@ -97,7 +109,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("ln_fwd", "rms_fwd", "ln_bwd", "rms_bwd", "ln_fwd_ex", "rms_fwd_ex", "ln_bwd_ex", "rms_bwd_ex",
                  "ln_bwd_rows", "rms_bwd_rows",
                  "gbn_bwd_reduce", "gbn_bwd_plan", "gbn_device_error", "silu_bwd", "gelu_bwd",
-                 "ln_bwd_host", "rms_bwd_host", "silu_bwd_host", "gelu_bwd_host"):
+                 "ln_bwd_host", "rms_bwd_host", "silu_bwd_host", "gelu_bwd_host", "ln_bwd_host_ex",
+                 "rms_bwd_host_ex", "silu_bwd_host_ex", "gelu_bwd_host_ex"):
         getattr(L, name).restype = _int
     return L
 
@@ -202,17 +215,23 @@ def device_error(clear: bool = True, device=None) -> int:
         return int(lib().gbn_device_error(int(clear)))
 
 
-def _options(ld_x: int, ld_dy: int, ld_out: int, accumulate: bool = False, grad_dtype=torch.float32,
-             reduce: str = "partials"):
-    return GbnOptions(ld_x, ld_dy, ld_out, int(bool(accumulate)), DTYPE_CODES[grad_dtype], REDUCE_MODES[reduce])
+def _options(ld_x: int = 0, ld_dy: int = 0, ld_out: int = 0, accumulate: bool = False, grad_dtype=torch.float32,
+             reduce: str = "partials", kernel: str = "auto", host_chunk: int = 0, wait_limit_ns: int = 0):
+    return GbnOptions(ld_x, ld_dy, ld_out, int(bool(accumulate)), DTYPE_CODES[grad_dtype], REDUCE_MODES[reduce],
+                      KERNELS[kernel], int(host_chunk), int(wait_limit_ns))
+
+
+def _host_options(host_chunk: int = 0):
+    return GbnOptions(0, 0, 0, 0, 0, 0, 0, int(host_chunk), 0)
 
 
 def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float, *,
            y: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
-           rstd: Optional[torch.Tensor] = None, stream=None):
+           rstd: Optional[torch.Tensor] = None, kernel: str = "auto", stream=None):
     """LayerNorm forward over the last dimension. Returns (y, mean, rstd).
 
-    x may be a 2-D view with contiguous rows (any row stride); y likewise."""
+    x may be a 2-D view with contiguous rows (any row stride); y likewise.
+    kernel: "auto", or "slot" / "plain" to force that kernel (KERNELS)."""
     M, N, ld_x = _rows_ld(x, "x")
     y = torch.empty(x.shape, dtype=x.dtype, device=x.device) if y is None else y
     mean = torch.empty(M, dtype=torch.float32, device=x.device) if mean is None else mean
@@ -222,7 +241,7 @@ def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
     _vec(mean, "mean", M, torch.float32, x.device)
     _vec(rstd, "rstd", M, torch.float32, x.device)
     ld_y = _same_rows(y, x, "y")
-    opt = _options(ld_x, N, ld_y)
+    opt = _options(ld_x, N, ld_y, kernel=kernel)
     with torch.cuda.device(x.device):
         _check("ln_fwd", lib().ln_fwd_ex(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
                                          float(eps), M, N, _code(x), ctypes.byref(opt), _stream(x.device, stream)))
@@ -230,7 +249,7 @@ def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
 
 
 def rms_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, *, y: Optional[torch.Tensor] = None,
-            rstd: Optional[torch.Tensor] = None, stream=None):
+            rstd: Optional[torch.Tensor] = None, kernel: str = "auto", stream=None):
     """RMSNorm forward over the last dimension. Returns (y, rstd)."""
     M, N, ld_x = _rows_ld(x, "x")
     y = torch.empty(x.shape, dtype=x.dtype, device=x.device) if y is None else y
@@ -238,7 +257,7 @@ def rms_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, *, y: Optional[tor
     _vec(gamma, "gamma", N, x.dtype, x.device)
     _vec(rstd, "rstd", M, torch.float32, x.device)
     ld_y = _same_rows(y, x, "y")
-    opt = _options(ld_x, N, ld_y)
+    opt = _options(ld_x, N, ld_y, kernel=kernel)
     with torch.cuda.device(x.device):
         _check("rms_fwd", lib().rms_fwd_ex(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), float(eps), M, N, _code(x),
                                            ctypes.byref(opt), _stream(x.device, stream)))
@@ -286,11 +305,13 @@ def _recompute_eps(stats, eps):
 def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: Optional[torch.Tensor],
            rstd: Optional[torch.Tensor], *, dx=None, dgamma=None, dbeta=None, workspace=None,
            accumulate: bool = False, grad_dtype=torch.float32, eps: Optional[float] = None,
-           reduce: str = "partials", stream=None):
+           reduce: str = "partials", kernel: str = "auto", wait_limit_ns: int = 0, stream=None):
     """LayerNorm backward from the saved mean / rstd. Returns (dx, dgamma, dbeta).
 
     reduce: "partials" (deterministic, the default), or the measurement
-    ablations "atomic" (nondeterministic) and "colwalk".
+    ablations "atomic" (nondeterministic) and "colwalk".  kernel: "auto", or
+    "slot" / "plain" to force that kernel.  wait_limit_ns: the kernels' wait
+    limit (0 = two seconds), a diagnostic of the error path.
 
     With mean = rstd = None nothing was saved: the statistics are formed from
     x with ``eps``.  dgamma / dbeta are float32 unless grad_dtype is x's
@@ -303,7 +324,7 @@ def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: Optiona
     dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
     dbeta = _grads(dbeta, "dbeta", N, grad_dtype, x.device, accumulate)
     workspace, wsb = _workspace(workspace, M, N, x, True)
-    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype, reduce)
+    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype, reduce, kernel, 0, wait_limit_ns)
     with torch.cuda.device(x.device):
         _check("ln_bwd", lib().ln_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
                                          _ptr(dgamma), _ptr(dbeta), eps_arg, M, N, _code(x), _ptr(workspace), wsb,
@@ -313,7 +334,8 @@ def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: Optiona
 
 def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: Optional[torch.Tensor], *,
             dx=None, dgamma=None, workspace=None, accumulate: bool = False, grad_dtype=torch.float32,
-            eps: Optional[float] = None, reduce: str = "partials", stream=None):
+            eps: Optional[float] = None, reduce: str = "partials", kernel: str = "auto", wait_limit_ns: int = 0,
+            stream=None):
     """RMSNorm backward from the saved rstd (None: recomputed from x with eps).
     Returns (dx, dgamma); options as for ln_bwd."""
     if grad_dtype not in (torch.float32, x.dtype):
@@ -322,7 +344,7 @@ def rms_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: Option
     M, N, dx, (ld_x, ld_dy, ld_dx) = _bwd_args(dy, x, gamma, (("rstd", rstd),), dx)
     dgamma = _grads(dgamma, "dgamma", N, grad_dtype, x.device, accumulate)
     workspace, wsb = _workspace(workspace, M, N, x, False)
-    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype, reduce)
+    opt = _options(ld_x, ld_dy, ld_dx, accumulate, grad_dtype, reduce, kernel, 0, wait_limit_ns)
     with torch.cuda.device(x.device):
         _check("rms_bwd", lib().rms_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
                                            eps_arg, M, N, _code(x), _ptr(workspace), wsb, ctypes.byref(opt),
@@ -397,10 +419,14 @@ def gelu_bwd(dy: torch.Tensor, preact: torch.Tensor, *, dx: Optional[torch.Tenso
 # ---------------------------------------------------------------------------
 # backward from host buffers (copies pipelined with the kernels)
 # ---------------------------------------------------------------------------
-def bwd_host_workspace_bytes(M: int, N: int, dtype: torch.dtype, has_beta: bool, device=None) -> int:
-    """Device workspace bytes ``ln_bwd_host`` / ``rms_bwd_host`` need."""
+def bwd_host_workspace_bytes(M: int, N: int, dtype: torch.dtype, has_beta: bool, device=None,
+                             chunk_rows: int = 0) -> int:
+    """Device workspace bytes ``ln_bwd_host`` / ``rms_bwd_host`` need (for
+    ``chunk_rows`` rows per chunk; 0 = about 16 MiB of each input)."""
+    opt = _host_options(chunk_rows)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        return int(lib().gbn_bwd_host_workspace_bytes(M, N, DTYPE_CODES[dtype], int(has_beta)))
+        return int(lib().gbn_bwd_host_workspace_bytes_ex(M, N, DTYPE_CODES[dtype], int(has_beta),
+                                                         ctypes.byref(opt)))
 
 
 def _host_args(fn, dy, x, gamma, stats, dx, grads):
@@ -429,8 +455,8 @@ def _host_args(fn, dy, x, gamma, stats, dx, grads):
     return M, N, dx, out
 
 
-def _host_workspace(workspace, M, N, dtype, ln, device):
-    need = bwd_host_workspace_bytes(M, N, dtype, ln, device)
+def _host_workspace(workspace, M, N, dtype, ln, device, chunk_rows):
+    need = bwd_host_workspace_bytes(M, N, dtype, ln, device, chunk_rows)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
     if workspace.device != torch.device(device) or workspace.numel() * workspace.element_size() < need:
@@ -439,37 +465,41 @@ def _host_workspace(workspace, M, N, dtype, ln, device):
 
 
 def ln_bwd_host(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor, *,
-                dx=None, dgamma=None, dbeta=None, workspace=None, device=None, stream=None):
+                dx=None, dgamma=None, dbeta=None, workspace=None, device=None, chunk_rows: int = 0, stream=None):
     """LayerNorm backward with every tensor in host memory (pinned for
     overlap).  Returns (dx, dgamma, dbeta) as CPU tensors, complete once
-    ``stream`` is."""
+    ``stream`` is.  chunk_rows: rows per pipeline chunk (0 = about 16 MiB of
+    each input)."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     M, N, dx, (dgamma, dbeta) = _host_args("ln_bwd_host", dy, x, gamma, (("mean", mean), ("rstd", rstd)), dx,
                                            (("dgamma", dgamma), ("dbeta", dbeta)))
-    workspace, wsb = _host_workspace(workspace, M, N, x.dtype, True, device)
+    workspace, wsb = _host_workspace(workspace, M, N, x.dtype, True, device, chunk_rows)
+    opt = _host_options(chunk_rows)
     with torch.cuda.device(device):
-        _check("ln_bwd_host", lib().ln_bwd_host(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
-                                                _ptr(dgamma), _ptr(dbeta), M, N, _code(x), _ptr(workspace), wsb,
-                                                _stream(device, stream)))
+        _check("ln_bwd_host", lib().ln_bwd_host_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd),
+                                                   _ptr(dx), _ptr(dgamma), _ptr(dbeta), M, N, _code(x),
+                                                   _ptr(workspace), wsb, ctypes.byref(opt),
+                                                   _stream(device, stream)))
     return dx, dgamma, dbeta
 
 
 def rms_bwd_host(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: torch.Tensor, *,
-                 dx=None, dgamma=None, workspace=None, device=None, stream=None):
+                 dx=None, dgamma=None, workspace=None, device=None, chunk_rows: int = 0, stream=None):
     """RMSNorm backward with every tensor in host memory (pinned for
     overlap).  Returns (dx, dgamma) as CPU tensors, complete once ``stream``
-    is."""
+    is.  chunk_rows as for ln_bwd_host."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     M, N, dx, (dgamma,) = _host_args("rms_bwd_host", dy, x, gamma, (("rstd", rstd),), dx, (("dgamma", dgamma),))
-    workspace, wsb = _host_workspace(workspace, M, N, x.dtype, False, device)
+    workspace, wsb = _host_workspace(workspace, M, N, x.dtype, False, device, chunk_rows)
+    opt = _host_options(chunk_rows)
     with torch.cuda.device(device):
-        _check("rms_bwd_host", lib().rms_bwd_host(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
-                                                  _ptr(dgamma), M, N, _code(x), _ptr(workspace), wsb,
-                                                  _stream(device, stream)))
+        _check("rms_bwd_host", lib().rms_bwd_host_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
+                                                     _ptr(dgamma), M, N, _code(x), _ptr(workspace), wsb,
+                                                     ctypes.byref(opt), _stream(device, stream)))
     return dx, dgamma
 
 
-def _act_host(fn: str, dy: torch.Tensor, preact: torch.Tensor, dx, workspace, device, stream):
+def _act_host(fn: str, dy: torch.Tensor, preact: torch.Tensor, dx, workspace, device, chunk, stream):
     for name, t in (("dy", dy), ("preact", preact)):
         if t.device.type != "cpu" or not t.is_contiguous():
             raise ValueError(f"{fn}: {name} must be a contiguous CPU tensor")
@@ -481,24 +511,28 @@ def _act_host(fn: str, dy: torch.Tensor, preact: torch.Tensor, dx, workspace, de
     elif dx.device.type != "cpu" or not dx.is_contiguous() or dx.shape != dy.shape or dx.dtype != dy.dtype:
         raise ValueError(f"{fn}: dx must be a contiguous CPU tensor like dy")
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    opt = _host_options(chunk)
     with torch.cuda.device(device):
-        need = int(lib().gbn_act_host_workspace_bytes(dy.numel(), code))
+        need = int(lib().gbn_act_host_workspace_bytes_ex(dy.numel(), code, ctypes.byref(opt)))
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         wsb = workspace.numel() * workspace.element_size()
         if workspace.device != device or wsb < need:
             raise ValueError(f"{fn}: workspace must be a device buffer of at least {need} bytes")
-        _check(fn, getattr(lib(), fn)(_ptr(dy), _ptr(preact), _ptr(dx), dy.numel(), code, _ptr(workspace), wsb,
-                                      _stream(device, stream)))
+        _check(fn, getattr(lib(), fn + "_ex")(_ptr(dy), _ptr(preact), _ptr(dx), dy.numel(), code, _ptr(workspace),
+                                              wsb, ctypes.byref(opt), _stream(device, stream)))
     return dx
 
 
-def silu_bwd_host(dy: torch.Tensor, preact: torch.Tensor, *, dx=None, workspace=None, device=None, stream=None):
+def silu_bwd_host(dy: torch.Tensor, preact: torch.Tensor, *, dx=None, workspace=None, device=None,
+                  chunk: int = 0, stream=None):
     """silu_bwd with dy, preact and dx in host memory (pinned for overlap);
-    dx is complete once ``stream`` is."""
-    return _act_host("silu_bwd_host", dy, preact, dx, workspace, device, stream)
+    dx is complete once ``stream`` is.  chunk: elements per pipeline chunk
+    (0 = about 16 MiB of each tensor)."""
+    return _act_host("silu_bwd_host", dy, preact, dx, workspace, device, chunk, stream)
 
 
-def gelu_bwd_host(dy: torch.Tensor, preact: torch.Tensor, *, dx=None, workspace=None, device=None, stream=None):
+def gelu_bwd_host(dy: torch.Tensor, preact: torch.Tensor, *, dx=None, workspace=None, device=None,
+                  chunk: int = 0, stream=None):
     """gelu_bwd with dy, preact and dx in host memory (pinned for overlap)."""
-    return _act_host("gelu_bwd_host", dy, preact, dx, workspace, device, stream)
+    return _act_host("gelu_bwd_host", dy, preact, dx, workspace, device, chunk, stream)

@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(ActShape<ACT>::kThreads, 1) act_bwd_kernel(con
         // flight before the CTA's shared memory is released
         if (lane == 0) {
             for (int64_t kk = k; kk < issued; ++kk) {
-                if (!mbar_wait_bounded(&bar[kk % S], static_cast<uint32_t>((kk / S) & 1), 100000000ull)) {
+                if (!mbar_wait_bounded(&bar[kk % S], static_cast<uint32_t>((kk / S) & 1), kDrainNs)) {
                     record_error(p.err, kErrDrain);
                     break;
                 }

@@ -8,8 +8,8 @@ cudaError_t launch_bwd_staged_bf16(bool ln, int nv, bool full, const BwdParams &
     return bwd_staged_dispatch<__nv_bfloat16>(ln, nv, full, p, smem, s);
 }
 
-cudaError_t launch_bwd_ws_bf16(bool ln, int vo, const BwdParams &p, int threads, size_t smem, cudaStream_t s) {
-    return bwd_ws_dispatch<__nv_bfloat16>(ln, vo, p, threads, smem, s);
+cudaError_t launch_bwd_ws_bf16(bool ln, int vo, const BwdParams &p, size_t smem, cudaStream_t s) {
+    return bwd_ws_dispatch<__nv_bfloat16>(ln, vo, p, smem, s);
 }
 
 cudaError_t launch_bwd_plain_bf16(bool ln, const BwdParams &p, cudaStream_t s) { return bwd_plain_dispatch<__nv_bfloat16>(ln, p, s); }

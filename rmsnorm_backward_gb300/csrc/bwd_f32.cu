@@ -8,8 +8,8 @@ cudaError_t launch_bwd_staged_f32(bool ln, int nv, bool full, const BwdParams &p
     return bwd_staged_dispatch<float>(ln, nv, full, p, smem, s);
 }
 
-cudaError_t launch_bwd_ws_f32(bool ln, int vo, const BwdParams &p, int threads, size_t smem, cudaStream_t s) {
-    return bwd_ws_dispatch<float>(ln, vo, p, threads, smem, s);
+cudaError_t launch_bwd_ws_f32(bool ln, int vo, const BwdParams &p, size_t smem, cudaStream_t s) {
+    return bwd_ws_dispatch<float>(ln, vo, p, smem, s);
 }
 
 cudaError_t launch_bwd_plain_f32(bool ln, const BwdParams &p, cudaStream_t s) { return bwd_plain_dispatch<float>(ln, p, s); }

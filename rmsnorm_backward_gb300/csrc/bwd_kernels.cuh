@@ -174,14 +174,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
         const int64_t row = row0 + slot + (int64_t)issued * slots;
         unsigned char *dst = ring + (size_t)pst * stage_bytes;
         mbar_arrive_expect_tx(&bar[pst], stage_bytes);
-        if (p.l2_hint) {
-            const uint64_t pol = policy_evict_first();
-            bulk_load(dst, static_cast<const T *>(p.x) + row * p.ld_x, rowb, &bar[pst], pol);
-            bulk_load(dst + rowb, static_cast<const T *>(p.dy) + row * p.ld_dy, rowb, &bar[pst], pol);
-        } else {
-            bulk_load_nohint(dst, static_cast<const T *>(p.x) + row * p.ld_x, rowb, &bar[pst]);
-            bulk_load_nohint(dst + rowb, static_cast<const T *>(p.dy) + row * p.ld_dy, rowb, &bar[pst]);
-        }
+        bulk_load_nohint(dst, static_cast<const T *>(p.x) + row * p.ld_x, rowb, &bar[pst]);
+        bulk_load_nohint(dst + rowb, static_cast<const T *>(p.dy) + row * p.ld_dy, rowb, &bar[pst]);
         if (++pst == S) pst = 0;
         ++issued;
     };
@@ -235,7 +229,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     RingPos pos;
     int k = 0;
     for (; k < ns; ++k) {
-        const bool timed_out = !mbar_wait_bounded(&bar[pos.stage], pos.parity);
+        const bool timed_out = !mbar_wait_bounded(&bar[pos.stage], pos.parity, p.wait_ns);
         if (timed_out) record_error(p.err, kErrWaitFull);
         if constexpr (RECOMP && MODE == kHoldAll) {
             // No saved statistics, row held in registers: x and dy in fp32.
@@ -436,7 +430,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
     // (bounded) before the CTA exits
     if (ts == 0) {
         for (int kk = k; kk < issued; ++kk) {
-            if (!mbar_wait_bounded(&bar[kk % S], (kk / S) & 1, 100000000ull)) {
+            if (!mbar_wait_bounded(&bar[kk % S], (kk / S) & 1, kDrainNs)) {
                 record_error(p.err, kErrDrain);
                 break;
             }

@@ -9,33 +9,36 @@
 
 namespace gbn {
 
-constexpr int kSumWarps = 5;
+// warps of each role: one producer, kSumWarps sum warps (every row's sums
+// split over all of them), kOutWarps output warps (fixed column slices)
+constexpr int kSumWarps = 4;
+constexpr int kOutWarps = 16;
+constexpr int kWsThreads = 32 * (1 + kSumWarps + kOutWarps);
 
 struct WsLayout {
-    size_t gam, stat, cval, bars, total;
+    size_t gam, cval, xch, bars, total;
 };
 
-// ring [S][2 * rowb] | gamma [rowb] | rstd, mean [stat_rows] | sums [S][2], issued count |
-// full, ready, consumed [S]
-__host__ __device__ inline WsLayout ws_layout(bool ln, size_t rowb, int S, int stat_rows) {
+// ring [S][2 * rowb] | gamma [rowb] | per stage: the sum warps' partial sums
+// [S][kSumWarps] float4 and the row's statistics [S] float4 |
+// save-nothing LayerNorm exchange [2][kSumWarps] floats + abort flags [2] |
+// mbarriers full, ready, consumed [S] and gamma's
+__host__ __device__ inline WsLayout ws_layout(size_t rowb, int S) {
     WsLayout L;
     L.gam = (size_t)S * 2 * rowb;
-    L.stat = L.gam + round_up(rowb, 16);
-    L.cval = L.stat + round_up((size_t)stat_rows * 4 * (ln ? 2 : 1), 16);
-    L.bars = L.cval + round_up((size_t)S * 2 * 4 + 4, 16);
-    L.total = L.bars + (size_t)3 * S * 8;
+    L.cval = L.gam + round_up(rowb, 16);
+    L.xch = L.cval + (size_t)S * (kSumWarps + 1) * 16;
+    L.bars = L.xch + round_up((size_t)2 * kSumWarps * 4 + 8, 16);
+    L.total = L.bars + ((size_t)3 * S + 1) * 8;
     return L;
 }
 
-// output warps and 16-byte vectors per lane for a row of nvec vectors
-__host__ __device__ inline bool ws_shape(int nvec, int *out_warps, int *vec_per_lane) {
-    if (nvec % 32 != 0) return false;
-    const int lanes = nvec / 32;  // vectors per lane if one warp held the row
-    const int no = lanes < 16 ? lanes : 16;
-    if (lanes % no != 0) return false;
-    const int vo = lanes / no;
+// 16-byte vectors per output lane for a row of nvec vectors: the row must
+// split into kOutWarps warps x 32 lanes x 1 or 2 vectors
+__host__ __device__ inline bool ws_shape(int nvec, int *vec_per_lane) {
+    if (nvec % (32 * kOutWarps) != 0) return false;
+    const int vo = nvec / (32 * kOutWarps);
     if (vo != 1 && vo != 2) return false;
-    *out_warps = no;
     *vec_per_lane = vo;
     return true;
 }

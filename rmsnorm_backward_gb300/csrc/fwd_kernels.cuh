@@ -70,17 +70,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
     if (ts == 0) *flag = 0;
     __syncthreads();
 
-    const uint64_t pol = policy_evict_first();
     const size_t row_step = (size_t)slots * p.ld_y;
     const size_t xrow_step = (size_t)slots * p.ld_x;
     const T *px = static_cast<const T *>(p.x) + (row0 + slot) * p.ld_x;
     int issued = 0, pst = 0;
     auto issue = [&]() {
         mbar_arrive_expect_tx(&bar[pst], rowb);
-        if (p.l2_hint)
-            bulk_load(ring + (size_t)pst * rowb, px, rowb, &bar[pst], pol);
-        else
-            bulk_load_nohint(ring + (size_t)pst * rowb, px, rowb, &bar[pst]);
+        bulk_load_nohint(ring + (size_t)pst * rowb, px, rowb, &bar[pst]);
         px += xrow_step;
         if (++pst == S) pst = 0;
         ++issued;
@@ -204,7 +200,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) fwd_staged_kernel(const FwdPa
     // (bounded) before the CTA exits
     if (ts == 0) {
         for (int kk = k; kk < issued; ++kk) {
-            if (!mbar_wait_bounded(&bar[kk % S], (kk / S) & 1, 100000000ull)) {
+            if (!mbar_wait_bounded(&bar[kk % S], (kk / S) & 1, kDrainNs)) {
                 record_error(p.err, kErrDrain);
                 break;
             }

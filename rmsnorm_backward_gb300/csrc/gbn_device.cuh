@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gbn_launch.h"
+
 namespace gbn {
 
 // ---------------------------------------------------------------------------
@@ -149,65 +151,50 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// a counter in shared memory written by one thread and polled by others
-__device__ __forceinline__ void st_release_shared(int *p, int v) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire_shared(const int *p) {
-    int v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
-    return v;
-}
-
-// Waits until *counter > k, giving up after ~limit_ns.  Returns false on giving up.
-__device__ __forceinline__ bool wait_counter_above(const int *counter, int k, uint64_t limit_ns = 2000000000ull) {
-    if (ld_acquire_shared(counter) > k) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1; it < (1u << 28); ++it) {
-        if (ld_acquire_shared(counter) > k) return true;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
-    }
-    return false;
+// non-blocking look at whether the phase with the given parity completed
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 // Waits for the phase of `bar` with the given parity to complete, giving up
-// after ~limit_ns (checked on the global timer) or 2^28 polls, whichever
-// comes first.  Returns false on giving up.
+// after ~limit_ns (checked on the global timer before the first suspending
+// poll and every 64 polls after it) or 2^28 polls, whichever comes first.
+// Returns false on giving up.  The first look does not suspend, so a limit
+// far below a copy's latency gives up at once on a phase still open.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                                  uint64_t limit_ns = kWaitNs) {
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1; it < (1u << 28); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
         if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if (mbar_try_wait(bar, parity)) return true;
     }
     return false;
+}
+
+// mbar_wait_bounded by every lane of a warp, with one outcome for the warp:
+// false if any lane gave up, so that the warp stops as a whole and no lane
+// is left behind in a later warp-wide shuffle or __syncwarp
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const bool ok = mbar_wait_bounded(bar, parity, limit_ns);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // 1-D bulk copy global -> this CTA's shared memory, completing `bytes` of
 // transaction count on `bar`.  dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                          uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-// 1-D bulk copy without an L2 cache hint
 __device__ __forceinline__ void bulk_load_nohint(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
-}
-
-// L2 policy for data read exactly once (evict first)
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // programmatic dependent launch: let the next kernel on the stream launch

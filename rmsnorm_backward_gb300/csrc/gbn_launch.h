@@ -17,6 +17,10 @@ constexpr int kGenericThreads = 256;
 constexpr int kMaxRowsPerCta = 2048;
 // most 16-byte vectors one thread holds per row in the staged kernels
 constexpr int kMaxVecPerThread = 4;
+// default limit of a wait on another warp or on a bulk copy, and the limit
+// of the wait for a CTA's own copies still in flight before it exits
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
 
 struct FwdParams {
     const void *x;
@@ -33,7 +37,6 @@ struct FwdParams {
     int stages;     // staged: ring stages per row slot
     int stat_rows;  // unused by the forward (kept for a uniform layout)
     int *err;       // the device's error flag
-    int l2_hint;    // bulk loads carry an L2 evict-first hint
     int64_t ld_x;   // row strides, in elements, of x and y
     int64_t ld_y;
 };
@@ -55,7 +58,7 @@ struct BwdParams {
     int stages;
     int stat_rows;      // capacity, in rows, of the staged statistics
     int *err;           // the device's error flag
-    int l2_hint;        // bulk loads carry an L2 evict-first hint
+    uint64_t wait_ns;   // limit of the waits between warps and on bulk copies
     int64_t ld_x;       // row strides, in elements, of x, dy and dx
     int64_t ld_dy;
     int64_t ld_dx;
@@ -122,7 +125,7 @@ cudaError_t launch_bwd_staged(int dtype, bool ln, int nv, bool full, const BwdPa
                               cudaStream_t s);
 cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_t s);
 // warp-specialised backward (bwd_ws.cuh): vo vectors per output lane
-cudaError_t launch_bwd_ws(int dtype, bool ln, int vo, const BwdParams &p, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_bwd_ws(int dtype, bool ln, int vo, const BwdParams &p, size_t smem, cudaStream_t s);
 // dgamma / dbeta from the partial rows; out_dtype is GBN_F32 or the storage
 // dtype of the parameters (rounded to nearest even); accumulate adds the
 // buffers' previous contents (widened) to the sums before the store

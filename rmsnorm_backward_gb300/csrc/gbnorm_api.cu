@@ -8,7 +8,6 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
-#include <cstdlib>
 
 #include "bwd_ws_layout.h"
 #include "gbn_launch.h"
@@ -61,23 +60,13 @@ bool valid_dtype(int dtype) { return dtype == GBN_F32 || dtype == GBN_F16 || dty
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Optional overrides for experiments: GBN_GRID forces G, GBN_WARPS_PER_ROW the
-// slot width, GBN_NO_FULL=1 the bounds-checked kernel variants, GBN_L2_HINT=1
-// bulk loads with an L2
-// evict-first hint (measured ~2 us slower on the 16384 x 4096 backward).
-int env_int(const char *name) {
-    const char *v = std::getenv(name);
-    return v ? std::atoi(v) : 0;
-}
-
 // Number of row blocks (CTAs) G: one per SM, more only when a block would
 // exceed kMaxRowsPerCta rows.  It depends on (M, SM count) only, so the
-// workspace size and the reduction order do not depend on buffer alignment.
+// workspace size and the column reduce's order do not depend on buffer
+// alignment or on the kernel that takes the rows.
 int grid_rows(int64_t M, const DevInfo &d) {
     if (M <= 0) return 0;
     int64_t G = d.sms;
-    const int forced = env_int("GBN_GRID");
-    if (forced > 0) G = forced;
     if (G > M) G = M;
     const int64_t min_g = (M + kMaxRowsPerCta - 1) / kMaxRowsPerCta;
     if (G < min_g) G = min_g;
@@ -113,10 +102,6 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
         caps[1] = !ln && 32 / V < kMaxVecPerThread ? 32 / V : kMaxVecPerThread;
     }
     int W = 0;
-    const int forced = env_int("GBN_WARPS_PER_ROW");
-    if (forced == 1 || forced == 2 || forced == 4 || forced == 8 || forced == 16) {
-        if ((int64_t)32 * forced * kMaxVecPerThread >= nvec) W = forced;
-    }
     for (int pass = 0; pass < 3 && !W; ++pass) {
         for (int w = 1; w <= kRingThreads / 32; w *= 2) {
             if ((int64_t)32 * w * caps[pass] >= nvec) {
@@ -130,8 +115,7 @@ StagedPlan staged_plan(bool bwd, bool ln, int dtype, int64_t M, int64_t N, int G
     P.nv = static_cast<int>((nvec + P.tpr - 1) / P.tpr);
     // exact tiling drops the bounds checks, except in the x-holding backward
     // mode, where the unchecked variant measured slower (register spills)
-    P.full = (int64_t)P.nv * P.tpr == nvec && env_int("GBN_NO_FULL") == 0 &&
-             !(bwd && bwd_hold_mode(ln, P.nv * V) == kHoldX && P.nv * V > 16);
+    P.full = (int64_t)P.nv * P.tpr == nvec && !(bwd && bwd_hold_mode(ln, P.nv * V) == kHoldX && P.nv * V > 16);
     P.stat_rows = static_cast<int>((M + G - 1) / G);
     const int slots = kRingThreads / P.tpr;
     // as many stages as fit, at most 16 per slot
@@ -168,15 +152,32 @@ int check_shape(int64_t M, int64_t N, int dtype) {
     return GBN_OK;
 }
 
-// gbn_options resolved: strides in elements, accumulate, dgamma/dbeta dtype
+// gbn_options resolved: strides in elements, accumulate, dgamma/dbeta dtype,
+// kernel choice, host-buffer chunk, wait limit
 struct Opts {
     int64_t ld_x = 0, ld_dy = 0, ld_out = 0;
     bool accumulate = false;
     int grad_dtype = GBN_F32;
     int reduce_mode = GBN_REDUCE_PARTIALS;
+    int kernel = GBN_KERNEL_AUTO;
+    int64_t host_chunk = 0;
+    uint64_t wait_ns = kWaitNs;
 };
 
+// fields every call reads: the kernel choice and the wait limit
+int resolve_common(const gbn_options *o, Opts *r) {
+    if (!o) return GBN_OK;
+    if (o->kernel < GBN_KERNEL_AUTO || o->kernel > GBN_KERNEL_PLAIN || o->wait_limit_ns < 0) return GBN_EINVAL;
+    r->kernel = o->kernel;
+    if (o->wait_limit_ns > 0) r->wait_ns = static_cast<uint64_t>(o->wait_limit_ns);
+    return GBN_OK;
+}
+
+// the device-buffer calls: everything but host_chunk
 int resolve_options(const gbn_options *o, int64_t N, int dtype, Opts *r) {
+    int st = resolve_common(o, r);
+    if (st != GBN_OK) return st;
+    if (o && o->host_chunk != 0) return GBN_EINVAL;
     r->ld_x = o && o->ld_x ? o->ld_x : N;
     r->ld_dy = o && o->ld_dy ? o->ld_dy : N;
     r->ld_out = o && o->ld_out ? o->ld_out : N;
@@ -188,6 +189,17 @@ int resolve_options(const gbn_options *o, int64_t N, int dtype, Opts *r) {
     r->reduce_mode = o ? o->reduce_mode : GBN_REDUCE_PARTIALS;
     if (r->reduce_mode < GBN_REDUCE_PARTIALS || r->reduce_mode > GBN_REDUCE_COLWALK) return GBN_EINVAL;
     if (r->reduce_mode != GBN_REDUCE_PARTIALS && r->grad_dtype != GBN_F32) return GBN_EDTYPE;
+    return GBN_OK;
+}
+
+// the host-buffer calls: host_chunk, kernel and the wait limit only
+int resolve_host_options(const gbn_options *o, Opts *r) {
+    int st = resolve_common(o, r);
+    if (st != GBN_OK) return st;
+    if (!o) return GBN_OK;
+    if (o->ld_x || o->ld_dy || o->ld_out || o->accumulate || o->grad_dtype || o->reduce_mode || o->host_chunk < 0)
+        return GBN_EINVAL;
+    r->host_chunk = o->host_chunk;
     return GBN_OK;
 }
 
@@ -212,12 +224,11 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
     FwdParams p{};
     p.x = x; p.gamma = gamma; p.beta = beta; p.y = y; p.mean = mean; p.rstd = rstd; p.eps = eps;
     p.M = M; p.N = static_cast<int>(N); p.G = grid_rows(M, d); p.err = d.err;
-    p.l2_hint = env_int("GBN_L2_HINT") != 0;
     p.ld_x = o.ld_x; p.ld_y = o.ld_out;
     const bool aligned = aligned16(x) && aligned16(y) && aligned16(gamma) && (!ln || aligned16(beta)) &&
                          stride16(o.ld_x, dtype) && stride16(o.ld_out, dtype);
     StagedPlan P;
-    if (aligned) P = staged_plan(false, ln, dtype, M, N, p.G, d);
+    if (aligned && o.kernel != GBN_KERNEL_PLAIN) P = staged_plan(false, ln, dtype, M, N, p.G, d);
     if (P.ok) {
         p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
         return cuda_status(launch_fwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
@@ -225,32 +236,28 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
     return cuda_status(launch_fwd_plain(dtype, ln, p, stream));
 }
 
-// The warp-specialised backward's launch (saved statistics, aligned buffers):
-// rows of 16 output warps x 32 lanes x 1-2 vectors, where it measured faster
-// (shorter rows leave too few output warps; at 4 vectors a lane, which
-// ws_shape refuses, the slot kernel was faster), and >= 2 stages.
+// The warp-specialised backward's launch: rows of 16 output warps x 32
+// lanes x 1-2 vectors, where it measured faster (shorter rows leave too few
+// output warps; at 4 vectors a lane the slot kernel was faster), and >= 2
+// stages.  It depends on the shape and the device only.
 struct WsPlan {
     bool ok = false;
-    int vo = 0, threads = 0, stages = 0, stat_rows = 0;
+    int vo = 0, stages = 0;
     size_t smem = 0;
 };
 
-WsPlan ws_plan(bool ln, int dtype, int64_t M, int64_t N, int G, const DevInfo &d) {
+WsPlan ws_plan(int dtype, int64_t N, const DevInfo &d) {
     WsPlan w;
     const int V = 16 / elem_bytes(dtype);
-    int no = 0, vo = 0;
-    if (env_int("GBN_NO_WS") != 0 || N % V != 0 || !ws_shape(static_cast<int>(N / V), &no, &vo) || no != 16)
-        return w;
+    int vo = 0;
+    if (N % V != 0 || !ws_shape(static_cast<int>(N / V), &vo)) return w;
     const size_t rowb = (size_t)N * elem_bytes(dtype);
-    const int stat_rows = static_cast<int>((M + G - 1) / G);
     for (int S = 16; S >= 2; --S) {
-        const WsLayout L = ws_layout(ln, rowb, S, stat_rows);
+        const WsLayout L = ws_layout(rowb, S);
         if (L.total <= static_cast<size_t>(d.smem_optin)) {
             w.ok = true;
             w.vo = vo;
-            w.threads = 32 * (1 + kSumWarps + no);
             w.stages = S;
-            w.stat_rows = stat_rows;
             w.smem = L.total;
             break;
         }
@@ -258,12 +265,20 @@ WsPlan ws_plan(bool ln, int dtype, int64_t M, int64_t N, int G, const DevInfo &d
     return w;
 }
 
+// Slices of the column reduce's CTAs: 8 (256 threads) where the
+// warp-specialised kernel takes the shape, so that they fit on an SM beside
+// it and start as soon as its grid completes; 16 (512 threads) beside the
+// other kernels, which leave no room for them.  A function of the shape and
+// the device only (not of alignment or options), so every call that reduces
+// the same [G, N] partial rows sums them in the same order.
+bool colsum_small(int dtype, int64_t N, const DevInfo &d) { return ws_plan(dtype, N, d).ok; }
+
 // recompute_eps >= 0: no saved statistics (mean / rstd null), the kernels
 // form them from x with this eps; < 0: the statistics are required.
 int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
                   void *dx, int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes_given,
                   const Opts &o, cudaStream_t stream, float recompute_eps = -1.f, float *dgamma = nullptr,
-                  float *dbeta = nullptr, float *part_g = nullptr, float *part_b = nullptr, int *kind = nullptr) {
+                  float *dbeta = nullptr, float *part_g = nullptr, float *part_b = nullptr) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (M == 0) return GBN_OK;
@@ -280,7 +295,7 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     p.part = part_g ? part_g : workspace_partials(workspace);
     p.part_b = part_b;
     p.M = M; p.N = static_cast<int>(N); p.ldp = partial_ld(N); p.G = grid_rows(M, d); p.err = d.err;
-    p.l2_hint = env_int("GBN_L2_HINT") != 0;
+    p.wait_ns = o.wait_ns;
     p.ld_x = o.ld_x; p.ld_dy = o.ld_dy; p.ld_dx = o.ld_out;
     p.eps = recompute ? recompute_eps : 0.f;
     if (o.reduce_mode == GBN_REDUCE_ATOMIC) {  // the caller zeroed them, unless accumulating
@@ -291,26 +306,22 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
                          stride16(o.ld_x, dtype) && stride16(o.ld_dy, dtype) && stride16(o.ld_out, dtype);
     // the warp-specialised kernel (every reduce mode, so dx does not depend on it)
     bool launched = false;
-    if (aligned && !recompute) {
-        const WsPlan w = ws_plan(ln, dtype, M, N, p.G, d);
+    if (aligned && o.kernel == GBN_KERNEL_AUTO) {
+        const WsPlan w = ws_plan(dtype, N, d);
         if (w.ok) {
             p.stages = w.stages;
-            p.stat_rows = w.stat_rows;
-            st = cuda_status(launch_bwd_ws(dtype, ln, w.vo, p, w.threads, w.smem, stream));
+            st = cuda_status(launch_bwd_ws(dtype, ln, w.vo, p, w.smem, stream));
             launched = true;
-            if (kind) *kind = 2;
         }
     }
     if (!launched) {
         StagedPlan P;
-        if (aligned) P = staged_plan(true, ln, dtype, M, N, p.G, d);
+        if (aligned && o.kernel != GBN_KERNEL_PLAIN) P = staged_plan(true, ln, dtype, M, N, p.G, d);
         if (P.ok) {
             p.tpr = P.tpr; p.stages = P.stages; p.stat_rows = P.stat_rows;
             st = cuda_status(launch_bwd_staged(dtype, ln, P.nv, P.full, p, P.smem, stream));
-            if (kind) *kind = 1;
         } else {
             st = cuda_status(launch_bwd_plain(dtype, ln, p, stream));
-            if (kind) *kind = 0;
         }
     }
     if (st == GBN_OK && o.reduce_mode == GBN_REDUCE_COLWALK)
@@ -318,12 +329,10 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     return st;
 }
 
-// rows_kind: the kernel that wrote the partial rows (2 warp-specialised, 1
-// slot, 0 plain), or -1 when unknown (the phase call), then taken from the
-// shape as the saved-statistics backward would choose it.  It picks the
-// reduce's CTA shape: small CTAs beside the warp-specialised kernel.
+// The column reduce of the partial rows in the workspace.  Its order is a
+// function of (M, N, dtype, device) only, whichever rows kernel ran.
 int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, int64_t N, int dtype, bool ln,
-                void *dgamma, void *dbeta, const Opts &o, cudaStream_t stream, int rows_kind = -1) {
+                void *dgamma, void *dbeta, const Opts &o, cudaStream_t stream) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (!dgamma || (ln && !dbeta)) return GBN_EINVAL;
@@ -339,10 +348,9 @@ int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, 
     if ((st = device_info(&d)) != GBN_OK) return st;
     if (workspace_bytes_given < workspace_bytes(M, N, ln, d)) return GBN_EWORKSPACE;
     const int G = grid_rows(M, d);
-    const bool small = rows_kind >= 0 ? rows_kind == 2 : ws_plan(ln, dtype, M, N, G, d).ok;
     return cuda_status(launch_colsum(workspace_partials(const_cast<void *>(workspace)), G, partial_ld(N),
                                      static_cast<int>(N), dgamma, ln ? dbeta : nullptr, o.grad_dtype,
-                                     o.accumulate, small, stream));
+                                     o.accumulate, colsum_small(dtype, N, d), stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -372,12 +380,12 @@ int64_t host_chunk_rows(int64_t R, int64_t i) {
     return i >= 4 || (r0 << i) >= R ? R : r0 << i;
 }
 
-HostPlan host_plan(int64_t M, int64_t N, int dtype, bool ln, const DevInfo &d) {
+// chunk_rows: rows per chunk after the ramp, 0 for about kHostChunkBytes of
+// each input
+HostPlan host_plan(int64_t M, int64_t N, int dtype, bool ln, int64_t chunk_rows, const DevInfo &d) {
     HostPlan h;
     const size_t rowb = (size_t)N * elem_bytes(dtype);
-    int64_t R = (int64_t)(kHostChunkBytes / rowb);
-    const int forced = env_int("GBN_HOST_CHUNK_ROWS");
-    if (forced > 0) R = forced;
+    int64_t R = chunk_rows > 0 ? chunk_rows : (int64_t)(kHostChunkBytes / rowb);
     if (R < 1) R = 1;
     if (R > M) R = M;
     h.R = R;
@@ -446,7 +454,7 @@ int host_streams(HostStreams *hs) {
 
 int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd,
                   void *dx, float *dgamma, float *dbeta, int64_t M, int64_t N, int dtype, void *workspace,
-                  size_t workspace_bytes_given, cudaStream_t s) {
+                  size_t workspace_bytes_given, const Opts &ho, cudaStream_t s) {
     int st = check_shape(M, N, dtype);
     if (st != GBN_OK) return st;
     if (!dgamma || (ln && !dbeta)) return GBN_EINVAL;
@@ -458,7 +466,7 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     if (!dy || !x || !gamma || !rstd || (ln && !mean) || !dx || !workspace) return GBN_EINVAL;
     DevInfo d;
     if ((st = device_info(&d)) != GBN_OK) return st;
-    const HostPlan h = host_plan(M, N, dtype, ln, d);
+    const HostPlan h = host_plan(M, N, dtype, ln, ho.host_chunk, d);
     if (workspace_bytes_given < h.total) return GBN_EWORKSPACE;
     HostStreams hs;
     if ((st = host_streams(&hs)) != GBN_OK) return st;
@@ -487,10 +495,9 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
               chk(cudaMemcpyAsync(base + h.gam, gamma, rowb, cudaMemcpyHostToDevice, hs.in)) &&
               chk(cudaMemcpyAsync(st_r, rstd, (size_t)M * 4, cudaMemcpyHostToDevice, hs.in)) &&
               (!ln || chk(cudaMemcpyAsync(st_m, mean, (size_t)M * 4, cudaMemcpyHostToDevice, hs.in)));
-    Opts o;
+    Opts o = ho;
     o.ld_x = o.ld_dy = o.ld_out = N;
     int64_t goff = 0, r0 = 0;
-    int last_kind = 0;
     for (int64_t i = 0; ok && i < h.nchunks; r0 += host_chunk_rows(h.R, i), ++i) {
         const int b = static_cast<int>(i % B);
         const int64_t want = host_chunk_rows(h.R, i), rows = M - r0 < want ? M - r0 : want;
@@ -508,8 +515,7 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
             const int G = grid_rows(rows, d);
             st = bwd_rows_impl(ln, base + h.dy[b], base + h.x[b], base + h.gam, ln ? st_m + r0 : nullptr, st_r + r0,
                                base + h.dx[b], rows, N, dtype, nullptr, 0, o, s, -1.f, nullptr, nullptr,
-                               part + (size_t)goff * ldp, ln ? part + (size_t)(h.Gtot + goff) * ldp : nullptr,
-                               &last_kind);
+                               part + (size_t)goff * ldp, ln ? part + (size_t)(h.Gtot + goff) * ldp : nullptr);
             goff += G;
             ok = st == GBN_OK && chk(cudaEventRecord(computed[b], s));
         }
@@ -521,7 +527,7 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     }
     if (ok) {
         ok = chk(launch_colsum(part, static_cast<int>(h.Gtot), ldp, static_cast<int>(N), grad,
-                               ln ? grad + N : nullptr, GBN_F32, false, last_kind == 2, s)) &&
+                               ln ? grad + N : nullptr, GBN_F32, false, colsum_small(dtype, N, d), s)) &&
              chk(cudaMemcpyAsync(dgamma, grad, (size_t)N * 4, cudaMemcpyDeviceToHost, s)) &&
              (!ln || chk(cudaMemcpyAsync(dbeta, grad + N, (size_t)N * 4, cudaMemcpyDeviceToHost, s))) &&
              chk(cudaEventRecord(dx_out, hs.out)) && chk(cudaStreamWaitEvent(s, dx_out, 0));
@@ -544,12 +550,12 @@ struct ActHostPlan {
     size_t dy[kHostBufs], pre[kHostBufs], dx[kHostBufs], total = 0;
 };
 
-ActHostPlan act_host_plan(int64_t n, int dtype) {
+// chunk: elements per chunk after the ramp, 0 for about kHostChunkBytes of
+// each tensor
+ActHostPlan act_host_plan(int64_t n, int dtype, int64_t chunk) {
     ActHostPlan h;
     const size_t es = elem_bytes(dtype);
-    int64_t R = (int64_t)(kHostChunkBytes / es);
-    const int forced = env_int("GBN_HOST_CHUNK_ROWS");  // elements here
-    if (forced > 0) R = forced;
+    int64_t R = chunk > 0 ? chunk : (int64_t)(kHostChunkBytes / es);
     if (R > n) R = n;
     if (R < 1) R = 1;
     h.R = R;
@@ -570,7 +576,7 @@ ActHostPlan act_host_plan(int64_t n, int dtype) {
 }
 
 int act_host_impl(int act, const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
-                  size_t workspace_bytes_given, cudaStream_t s) {
+                  size_t workspace_bytes_given, const Opts &ho, cudaStream_t s) {
     if (!valid_dtype(dtype)) return GBN_EDTYPE;
     if (n < 0) return GBN_EINVAL;
     if (n == 0) return GBN_OK;
@@ -578,7 +584,7 @@ int act_host_impl(int act, const void *dy, const void *preact, void *dx, int64_t
     DevInfo d;
     int st = device_info(&d);
     if (st != GBN_OK) return st;
-    const ActHostPlan h = act_host_plan(n, dtype);
+    const ActHostPlan h = act_host_plan(n, dtype, ho.host_chunk);
     if (workspace_bytes_given < h.total) return GBN_EWORKSPACE;
     HostStreams hs;
     if ((st = host_streams(&hs)) != GBN_OK) return st;
@@ -705,12 +711,10 @@ int ln_bwd_ex(const void *dy, const void *x, const void *gamma, const float *mea
         if (st == GBN_OK) st = cuda_status(cudaMemsetAsync(dbeta, 0, (size_t)N * 4, stream));
         if (st != GBN_OK) return st;
     }
-    int kind = 0;
     st = bwd_rows_impl(true, dy, x, gamma, mean, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
-                       recompute ? eps : -1.f, static_cast<float *>(dgamma), static_cast<float *>(dbeta), nullptr,
-                       nullptr, &kind);
+                       recompute ? eps : -1.f, static_cast<float *>(dgamma), static_cast<float *>(dbeta));
     if (st != GBN_OK || (M > 0 && o.reduce_mode != GBN_REDUCE_PARTIALS)) return st;
-    return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, o, stream, kind);
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, true, dgamma, dbeta, o, stream);
 }
 
 int rms_bwd_ex(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, void *dgamma,
@@ -729,11 +733,10 @@ int rms_bwd_ex(const void *dy, const void *x, const void *gamma, const float *rs
         st = cuda_status(cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream));
         if (st != GBN_OK) return st;
     }
-    int kind = 0;
     st = bwd_rows_impl(false, dy, x, gamma, nullptr, rstd, dx, M, N, dtype, workspace, workspace_bytes, o, stream,
-                       recompute ? eps : -1.f, static_cast<float *>(dgamma), nullptr, nullptr, nullptr, &kind);
+                       recompute ? eps : -1.f, static_cast<float *>(dgamma));
     if (st != GBN_OK || (M > 0 && o.reduce_mode != GBN_REDUCE_PARTIALS)) return st;
-    return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, o, stream, kind);
+    return reduce_impl(workspace, workspace_bytes, M, N, dtype, false, dgamma, nullptr, o, stream);
 }
 
 int ln_bwd(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
@@ -768,39 +771,83 @@ int gelu_bwd(const void *dy, const void *preact, void *dx, int64_t n, int dtype,
     return act_bwd_impl(kActGelu, dy, preact, dx, n, dtype, stream);
 }
 
-size_t gbn_bwd_host_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta) {
-    if (check_shape(M, N, dtype) != GBN_OK || M <= 0) return 0;
+size_t gbn_bwd_host_workspace_bytes_ex(int64_t M, int64_t N, int dtype, int has_beta, const gbn_options *opt) {
+    Opts o;
+    if (check_shape(M, N, dtype) != GBN_OK || M <= 0 || resolve_host_options(opt, &o) != GBN_OK) return 0;
     DevInfo d;
     if (device_info(&d) != GBN_OK) return 0;
-    return host_plan(M, N, dtype, has_beta != 0, d).total;
+    return host_plan(M, N, dtype, has_beta != 0, o.host_chunk, d).total;
+}
+
+size_t gbn_bwd_host_workspace_bytes(int64_t M, int64_t N, int dtype, int has_beta) {
+    return gbn_bwd_host_workspace_bytes_ex(M, N, dtype, has_beta, nullptr);
+}
+
+int ln_bwd_host_ex(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
+                   float *dgamma, float *dbeta, int64_t M, int64_t N, int dtype, void *workspace,
+                   size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream) {
+    Opts o;
+    const int st = resolve_host_options(opt, &o);
+    if (st != GBN_OK) return st;
+    return bwd_host_impl(true, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, M, N, dtype, workspace,
+                         workspace_bytes, o, stream);
+}
+
+int rms_bwd_host_ex(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, float *dgamma,
+                    int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes,
+                    const gbn_options *opt, cudaStream_t stream) {
+    Opts o;
+    const int st = resolve_host_options(opt, &o);
+    if (st != GBN_OK) return st;
+    return bwd_host_impl(false, dy, x, gamma, nullptr, rstd, dx, dgamma, nullptr, M, N, dtype, workspace,
+                         workspace_bytes, o, stream);
 }
 
 int ln_bwd_host(const void *dy, const void *x, const void *gamma, const float *mean, const float *rstd, void *dx,
                 float *dgamma, float *dbeta, int64_t M, int64_t N, int dtype, void *workspace,
                 size_t workspace_bytes, cudaStream_t stream) {
-    return bwd_host_impl(true, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, M, N, dtype, workspace,
-                         workspace_bytes, stream);
+    return ln_bwd_host_ex(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, M, N, dtype, workspace, workspace_bytes,
+                          nullptr, stream);
 }
 
 int rms_bwd_host(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx, float *dgamma,
                  int64_t M, int64_t N, int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    return bwd_host_impl(false, dy, x, gamma, nullptr, rstd, dx, dgamma, nullptr, M, N, dtype, workspace,
-                         workspace_bytes, stream);
+    return rms_bwd_host_ex(dy, x, gamma, rstd, dx, dgamma, M, N, dtype, workspace, workspace_bytes, nullptr,
+                           stream);
 }
 
-size_t gbn_act_host_workspace_bytes(int64_t n, int dtype) {
-    if (!valid_dtype(dtype) || n <= 0) return 0;
-    return act_host_plan(n, dtype).total;
+size_t gbn_act_host_workspace_bytes_ex(int64_t n, int dtype, const gbn_options *opt) {
+    Opts o;
+    if (!valid_dtype(dtype) || n <= 0 || resolve_host_options(opt, &o) != GBN_OK) return 0;
+    return act_host_plan(n, dtype, o.host_chunk).total;
+}
+
+size_t gbn_act_host_workspace_bytes(int64_t n, int dtype) { return gbn_act_host_workspace_bytes_ex(n, dtype, nullptr); }
+
+int silu_bwd_host_ex(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                     size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream) {
+    Opts o;
+    const int st = resolve_host_options(opt, &o);
+    if (st != GBN_OK) return st;
+    return act_host_impl(kActSilu, dy, preact, dx, n, dtype, workspace, workspace_bytes, o, stream);
+}
+
+int gelu_bwd_host_ex(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
+                     size_t workspace_bytes, const gbn_options *opt, cudaStream_t stream) {
+    Opts o;
+    const int st = resolve_host_options(opt, &o);
+    if (st != GBN_OK) return st;
+    return act_host_impl(kActGelu, dy, preact, dx, n, dtype, workspace, workspace_bytes, o, stream);
 }
 
 int silu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream) {
-    return act_host_impl(kActSilu, dy, preact, dx, n, dtype, workspace, workspace_bytes, stream);
+    return silu_bwd_host_ex(dy, preact, dx, n, dtype, workspace, workspace_bytes, nullptr, stream);
 }
 
 int gelu_bwd_host(const void *dy, const void *preact, void *dx, int64_t n, int dtype, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream) {
-    return act_host_impl(kActGelu, dy, preact, dx, n, dtype, workspace, workspace_bytes, stream);
+    return gelu_bwd_host_ex(dy, preact, dx, n, dtype, workspace, workspace_bytes, nullptr, stream);
 }
 
 int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *staged) {
@@ -812,7 +859,7 @@ int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *sta
     if (G) *G = g;
     if (staged) {
         *staged = 0;
-        if (M > 0 && ws_plan(has_beta != 0, dtype, M, N, g, d).ok)
+        if (M > 0 && ws_plan(dtype, N, d).ok)
             *staged = 2;
         else if (M > 0 && staged_plan(true, has_beta != 0, dtype, M, N, g, d).ok)
             *staged = 1;

@@ -58,15 +58,15 @@ cudaError_t launch_bwd_plain_f32(bool, const BwdParams &, cudaStream_t);
 cudaError_t launch_bwd_plain_f16(bool, const BwdParams &, cudaStream_t);
 cudaError_t launch_bwd_plain_bf16(bool, const BwdParams &, cudaStream_t);
 
-cudaError_t launch_bwd_ws_f32(bool, int, const BwdParams &, int, size_t, cudaStream_t);
-cudaError_t launch_bwd_ws_f16(bool, int, const BwdParams &, int, size_t, cudaStream_t);
-cudaError_t launch_bwd_ws_bf16(bool, int, const BwdParams &, int, size_t, cudaStream_t);
+cudaError_t launch_bwd_ws_f32(bool, int, const BwdParams &, size_t, cudaStream_t);
+cudaError_t launch_bwd_ws_f16(bool, int, const BwdParams &, size_t, cudaStream_t);
+cudaError_t launch_bwd_ws_bf16(bool, int, const BwdParams &, size_t, cudaStream_t);
 
-cudaError_t launch_bwd_ws(int dtype, bool ln, int vo, const BwdParams &p, int threads, size_t smem, cudaStream_t s) {
+cudaError_t launch_bwd_ws(int dtype, bool ln, int vo, const BwdParams &p, size_t smem, cudaStream_t s) {
     switch (dtype) {
-        case 0: return launch_bwd_ws_f32(ln, vo, p, threads, smem, s);
-        case 1: return launch_bwd_ws_f16(ln, vo, p, threads, smem, s);
-        case 2: return launch_bwd_ws_bf16(ln, vo, p, threads, smem, s);
+        case 0: return launch_bwd_ws_f32(ln, vo, p, smem, s);
+        case 1: return launch_bwd_ws_f16(ln, vo, p, smem, s);
+        case 2: return launch_bwd_ws_bf16(ln, vo, p, smem, s);
     }
     return cudaErrorInvalidValue;
 }

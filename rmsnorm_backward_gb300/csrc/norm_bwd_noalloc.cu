@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "gbnorm.h"
 
@@ -26,10 +27,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[GBN_NOALLOC_SCR
 constexpr int kMaxDevices = 64;
 void *g_scratch_ptr[kMaxDevices];
 std::atomic<int> g_scratch_ready[kMaxDevices];
+std::mutex g_scratch_mu;
 
 // The device address of this device's scratch array.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up
-// once per device, with that device current, and cached.
+// once per device, with that device current, and cached.  Host threads may
+// race on the first call: the cache is filled under a lock, and read
+// without one once its ready flag is seen.
 int scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -38,6 +42,11 @@ int scratch_address(void **out) {
     }
     if (dev < 0 || dev >= kMaxDevices) return GBN_ECUDA;
     if (!g_scratch_ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (g_scratch_ready[dev].load(std::memory_order_relaxed)) {
+            *out = g_scratch_ptr[dev];
+            return GBN_OK;
+        }
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) {

@@ -9,25 +9,44 @@ from typing import Dict, List, Optional
 import numpy as np
 import torch
 
+import guards
 import oracle
 import rmsnorm_backward_gb300 as gbn
 import tolerance as tol
 import workloads as wl
 
 
-def run_gpu(w: wl.Workload, inputs: Dict[str, torch.Tensor], device="cuda", stats_from_oracle=None):
-    """Forward then backward on the GPU. Returns CPU tensors."""
-    d = {k: v.to(device) for k, v in inputs.items()}
+def run_gpu(w: wl.Workload, inputs: Dict[str, torch.Tensor], device="cuda", kernel: str = "auto",
+            ws_misalign: int = 0):
+    """Forward then backward on the GPU. Returns CPU tensors.
+
+    Every input, output and the workspace sit between sentinel bands
+    (tests/guards.py); after the calls the bands and the inputs are checked
+    unchanged.  kernel: "auto", or "slot" / "plain" to force that kernel."""
+    g = guards.Guarded(device)
+    d = {k: g.copy_in(v, k) for k, v in inputs.items()}
+    M, N = w.M, w.N
+    tdt = wl.TORCH_DTYPES[w.dtype]
+    ln = w.op == "ln"
+    y = g.empty((M, N), tdt, "y")
+    rstd = g.empty((M,), torch.float32, "rstd")
+    mean = g.empty((M,), torch.float32, "mean") if ln else None
+    dx = g.empty((M, N), tdt, "dx")
+    dg = g.empty((N,), torch.float32, "dgamma")
+    db = g.empty((N,), torch.float32, "dbeta") if ln else None
+    ws = g.workspace(gbn.bwd_workspace_bytes(M, N, tdt, ln), misalign=ws_misalign)
     out = {}
-    if w.op == "ln":
-        y, mean, rstd = gbn.ln_fwd(d["x"], d["gamma"], d["beta"], w.eps)
-        dx, dg, db = gbn.ln_bwd(d["dy"], d["x"], d["gamma"], mean, rstd)
+    if ln:
+        gbn.ln_fwd(d["x"], d["gamma"], d["beta"], w.eps, y=y, mean=mean, rstd=rstd, kernel=kernel)
+        gbn.ln_bwd(d["dy"], d["x"], d["gamma"], mean, rstd, dx=dx, dgamma=dg, dbeta=db, workspace=ws,
+                   kernel=kernel)
         out.update(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db)
     else:
-        y, rstd = gbn.rms_fwd(d["x"], d["gamma"], w.eps)
-        dx, dg = gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd)
+        gbn.rms_fwd(d["x"], d["gamma"], w.eps, y=y, rstd=rstd, kernel=kernel)
+        gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd, dx=dx, dgamma=dg, workspace=ws, kernel=kernel)
         out.update(y=y, rstd=rstd, dx=dx, dgamma=dg)
     torch.cuda.synchronize()
+    g.check()
     return {k: v.cpu() for k, v in out.items()}
 
 
@@ -81,9 +100,10 @@ def compare(w: wl.Workload, inputs: Dict[str, torch.Tensor], got: Dict[str, torc
     return reps
 
 
-def assert_parity(w: wl.Workload, inputs: Optional[Dict[str, torch.Tensor]] = None, device="cuda"):
+def assert_parity(w: wl.Workload, inputs: Optional[Dict[str, torch.Tensor]] = None, device="cuda",
+                  kernel: str = "auto"):
     inputs = inputs if inputs is not None else wl.make_inputs(w)
-    got = run_gpu(w, inputs, device)
+    got = run_gpu(w, inputs, device, kernel)
     reps = compare(w, inputs, got)
     bad = [r for r in reps if not r.ok()]
     msg = f"{w.name} ({w.op} {w.dtype} {w.M}x{w.N}):\n  " + "\n  ".join(str(r) for r in reps)

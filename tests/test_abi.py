@@ -99,3 +99,39 @@ def test_activation_host_entry_checks(lib):
         assert fn(p, p, p, 8, 2, None, 1 << 20, None) == 1   # no workspace
         assert fn(p, p, p, -1, 2, p, 1 << 20, None) == 1     # negative size
         assert fn(p, p, p, 8, 9, p, 1 << 20, None) == 2      # unknown dtype
+
+
+def test_option_fields_are_checked_on_the_host(lib):
+    """gbn_options: an unknown kernel, a negative wait limit, a host chunk on
+    a device call, or a device-call field on a host-buffer call are
+    GBN_EINVAL before anything is enqueued (no GPU needed)."""
+    import rmsnorm_backward_gb300 as gbn
+    L = gbn._declare(ctypes.CDLL(gbn.library_path))
+    p = ctypes.c_void_p(16)
+
+    def opt(**kw):
+        o = gbn.GbnOptions()
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return ctypes.byref(o)
+
+    assert ctypes.sizeof(gbn.GbnOptions) == 56 and gbn.GbnOptions.host_chunk.offset == 40
+    for bad in (opt(kernel=3), opt(kernel=-1), opt(wait_limit_ns=-1), opt(host_chunk=64)):
+        assert L.rms_bwd_ex(p, p, p, p, p, p, 0.0, 4, 8, 2, p, 1 << 20, bad, None) == 1
+        assert L.rms_fwd_ex(p, p, p, p, 1e-5, 4, 8, 2, bad, None) == 1
+    for bad in (opt(ld_x=8), opt(accumulate=1), opt(grad_dtype=2), opt(reduce_mode=1), opt(host_chunk=-1),
+                opt(kernel=7)):
+        assert L.rms_bwd_host_ex(p, p, p, p, p, p, 4, 8, 2, p, 1 << 20, bad, None) == 1
+        assert L.ln_bwd_host_ex(p, p, p, p, p, p, p, p, 4, 8, 2, p, 1 << 20, bad, None) == 1
+        assert L.silu_bwd_host_ex(p, p, p, 8, 2, p, 1 << 20, bad, None) == 1
+        assert L.gbn_bwd_host_workspace_bytes_ex(4, 8, 2, 0, bad) == 0
+        assert L.gbn_act_host_workspace_bytes_ex(8, 2, bad) == 0
+
+
+def test_library_reads_no_environment():
+    """No knob of the environment reaches the library: which kernel runs
+    and the summation order of dgamma / dbeta depend only on the call."""
+    csrc = os.path.join(ROOT, "rmsnorm_backward_gb300", "csrc")
+    for name in os.listdir(csrc):
+        text = open(os.path.join(csrc, name)).read()
+        assert "getenv" not in text, f"{name} reads the environment"

@@ -131,20 +131,19 @@ def test_empty_and_argument_errors():
 
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_host_buffers_match_the_device_call(kind, dtype, monkeypatch):
+def test_host_buffers_match_the_device_call(kind, dtype):
     # small chunks, so the ramp and several chunks per buffer are exercised
-    monkeypatch.setenv("GBN_HOST_CHUNK_ROWS", "1000")
     a = _act(kind, dtype, 37, 1001)
     inp = wl.make_act_inputs(a)
     ref = FN[kind](inp["dy"].cuda(), inp["preact"].cuda()).cpu()
     host = {"silu": gbn.silu_bwd_host, "gelu": gbn.gelu_bwd_host}[kind]
-    dx = host(inp["dy"].pin_memory(), inp["preact"].pin_memory())
+    dx = host(inp["dy"].pin_memory(), inp["preact"].pin_memory(), chunk=1000)
     torch.cuda.synchronize()
     iv = torch.int32 if dtype == "f32" else torch.int16
     assert torch.equal(dx.view(iv), ref.view(iv))
     # in place over a pageable dy, on a side stream
     dy = inp["dy"].clone()
     s = torch.cuda.Stream()
-    out = host(dy, inp["preact"].clone(), dx=dy, stream=s)
+    out = host(dy, inp["preact"].clone(), dx=dy, chunk=1000, stream=s)
     s.synchronize()
     assert out.data_ptr() == dy.data_ptr() and torch.equal(dy.view(iv), ref.view(iv))

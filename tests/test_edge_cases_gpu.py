@@ -142,26 +142,65 @@ def test_exact_sums_are_bit_exact(op, M):
     assert np.array_equal(dgam.cpu().double().numpy(), dg_o)
 
 
+def _view(t: torch.Tensor, misalign: bool) -> torch.Tensor:
+    """t on the GPU, one element past a 16-byte boundary when misalign."""
+    if not misalign:
+        return t.cuda()
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device="cuda")
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
 @pytest.mark.parametrize("op", ["ln", "rms"])
-def test_two_phases_equal_the_fused_call(op):
-    w = _w(op, "bf16", 1000, 2048)
-    d = {k: v.cuda() for k, v in wl.make_inputs(w).items()}
+@pytest.mark.parametrize("N", [2048, 4096])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_two_phases_equal_the_fused_call(op, N, misalign):
+    """The phase calls (rows, then reduce) give the fused call's bits.  With
+    x and dy one element off a 16-byte boundary the rows go through the
+    plain kernel; the column reduce's order depends on the shape only, so
+    the phase call, which does not know the rows kernel, still matches."""
+    w = _w(op, "bf16", 1000, N)
+    inp = wl.make_inputs(w)
+    d = {k: v.cuda() for k, v in inp.items()}
+    x, dy = _view(inp["x"], misalign), _view(inp["dy"], misalign)
     ws = torch.empty(gbn.bwd_workspace_bytes(w.M, w.N, torch.bfloat16, op == "ln"), dtype=torch.uint8,
                      device="cuda")
     if op == "ln":
         y, mean, rstd = gbn.ln_fwd(d["x"], d["gamma"], d["beta"], w.eps)
-        dx, dg, db = gbn.ln_bwd(d["dy"], d["x"], d["gamma"], mean, rstd, workspace=ws)
-        dx2 = gbn.ln_bwd_rows(d["dy"], d["x"], d["gamma"], mean, rstd, workspace=ws)
+        dx, dg, db = gbn.ln_bwd(dy, x, d["gamma"], mean, rstd, workspace=ws)
+        dx2 = gbn.ln_bwd_rows(dy, x, d["gamma"], mean, rstd, dx=torch.empty_like(x), workspace=ws)
         dg2, db2 = torch.empty_like(dg), torch.empty_like(db)
         gbn.bwd_reduce(ws, w.M, w.N, torch.bfloat16, True, dgamma=dg2, dbeta=db2)
         assert torch.equal(db, db2)
     else:
         y, rstd = gbn.rms_fwd(d["x"], d["gamma"], w.eps)
-        dx, dg = gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd, workspace=ws)
-        dx2 = gbn.rms_bwd_rows(d["dy"], d["x"], d["gamma"], rstd, workspace=ws)
+        dx, dg = gbn.rms_bwd(dy, x, d["gamma"], rstd, workspace=ws)
+        dx2 = gbn.rms_bwd_rows(dy, x, d["gamma"], rstd, dx=torch.empty_like(x), workspace=ws)
         dg2 = torch.empty_like(dg)
         gbn.bwd_reduce(ws, w.M, w.N, torch.bfloat16, False, dgamma=dg2)
     assert torch.equal(dx.view(torch.int16), dx2.view(torch.int16)) and torch.equal(dg, dg2)
+    assert gbn.device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["rms_bf16_16384x4096", "ln_bf16_65536x1024", "rms_bf16_8192x16384"])
+def test_full_size_backward_is_bit_identical_over_ten_runs(name):
+    """The benchmarked sizes: ten backward calls on the same inputs give
+    the same dx, dgamma and dbeta bits (no atomics, one summation order)."""
+    w = wl.WORKLOADS[name]
+    d = {k: v.cuda() for k, v in wl.make_inputs(w).items()}
+    if w.op == "ln":
+        _, mean, rstd = gbn.ln_fwd(d["x"], d["gamma"], d["beta"], w.eps)
+        run = lambda: gbn.ln_bwd(d["dy"], d["x"], d["gamma"], mean, rstd)
+    else:
+        _, rstd = gbn.rms_fwd(d["x"], d["gamma"], w.eps)
+        run = lambda: gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd)
+    first = [t.clone() for t in run()]
+    for _ in range(9):
+        for a, b in zip(first, run()):
+            assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a.view(torch.int32),
+                               b.view(torch.int16) if b.dtype != torch.float32 else b.view(torch.int32))
+    assert gbn.device_error() == 0
 
 
 def test_non_default_stream():

@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import guards
 import oracle
 import rmsnorm_backward_gb300 as gbn
 import tolerance as tol
@@ -29,15 +30,26 @@ def _stats(w, inp):
     return None, rstd.cpu()
 
 
-def _host(w, inp, mean, rstd, pinned=True, **kw):
-    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
-    dy, x, g, rs = pin(inp["dy"]), pin(inp["x"]), pin(inp["gamma"]), pin(rstd)
+def _host(w, inp, mean, rstd, pinned=True, chunk_rows=0):
+    """The host-buffer call on guarded host buffers (inputs, outputs) and a
+    guarded device workspace; the bands and the inputs are checked after."""
+    gh, gd = guards.Guarded("cpu"), guards.Guarded("cuda")
+    dy, x, g = (gh.copy_in(inp[k], k, pin=pinned) for k in ("dy", "x", "gamma"))
+    rs = gh.copy_in(rstd, "rstd", pin=pinned)
+    M, N = w.M, w.N
+    dx = gh.empty((M, N), x.dtype, "dx", pin=pinned)
+    dg = gh.empty((N,), torch.float32, "dgamma", pin=pinned)
+    ws = gd.workspace(gbn.bwd_host_workspace_bytes(M, N, x.dtype, w.op == "ln", chunk_rows=chunk_rows))
     if w.op == "ln":
-        out = gbn.ln_bwd_host(dy, x, g, pin(mean), rs, **kw)
+        db = gh.empty((N,), torch.float32, "dbeta", pin=pinned)
+        out = gbn.ln_bwd_host(dy, x, g, gh.copy_in(mean, "mean", pin=pinned), rs, dx=dx, dgamma=dg, dbeta=db,
+                              workspace=ws, chunk_rows=chunk_rows)
     else:
-        out = gbn.rms_bwd_host(dy, x, g, rs, **kw)
+        out = gbn.rms_bwd_host(dy, x, g, rs, dx=dx, dgamma=dg, workspace=ws, chunk_rows=chunk_rows)
     torch.cuda.synchronize()
-    return out
+    gh.check()
+    gd.check()
+    return [t.clone() for t in out]
 
 
 def _device(w, inp, mean, rstd):
@@ -67,20 +79,18 @@ def _check_grads(w, inp, mean, rstd, got):
 @pytest.mark.parametrize("op", ["ln", "rms"])
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("M,N,chunk", [(1000, 512, 128), (300, 1000, 0), (37, 4096, 5), (513, 33, 64)])
-def test_host_matches_device_and_oracle(op, dtype, M, N, chunk, monkeypatch):
-    if chunk:
-        monkeypatch.setenv("GBN_HOST_CHUNK_ROWS", str(chunk))
+def test_host_matches_device_and_oracle(op, dtype, M, N, chunk):
     w = _w(op, dtype, M, N)
     inp = wl.make_inputs(w)
     mean, rstd = _stats(w, inp)
-    got = _host(w, inp, mean, rstd)
+    got = _host(w, inp, mean, rstd, chunk_rows=chunk)
     ref = _device(w, inp, mean, rstd)
     # every row goes through the same kernel arithmetic: dx is bit-identical
     assert torch.equal(got[0].view(torch.int16 if dtype != "f32" else torch.int32),
                        ref[0].view(torch.int16 if dtype != "f32" else torch.int32))
     _check_grads(w, inp, mean, rstd, got)
     # and the grouping of the partial sums is fixed: run to run identical
-    again = _host(w, inp, mean, rstd)
+    again = _host(w, inp, mean, rstd, chunk_rows=chunk)
     for a, b in zip(got[1:], again[1:]):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     assert gbn.device_error(clear=True) == 0
@@ -97,8 +107,7 @@ def test_host_headline_size(op):
     _check_grads(w, inp, mean, rstd, got)
 
 
-def test_pageable_in_place_side_stream_and_empty(monkeypatch):
-    monkeypatch.setenv("GBN_HOST_CHUNK_ROWS", "100")
+def test_pageable_in_place_side_stream_and_empty():
     w = _w("rms", "bf16", 700, 2048)
     inp = wl.make_inputs(w)
     _, rstd = _stats(w, inp)
@@ -106,7 +115,7 @@ def test_pageable_in_place_side_stream_and_empty(monkeypatch):
     # pageable host memory, dx written over dy, on a side stream
     dy, x, g, rs = tuple(inp[k].clone() for k in ("dy", "x", "gamma")) + (rstd.clone(),)
     s = torch.cuda.Stream()
-    dx, dg = gbn.rms_bwd_host(dy, x, g, rs, dx=dy, stream=s)
+    dx, dg = gbn.rms_bwd_host(dy, x, g, rs, dx=dy, chunk_rows=100, stream=s)
     s.synchronize()
     assert dx.data_ptr() == dy.data_ptr()
     assert torch.equal(dx.view(torch.int16), ref[0].view(torch.int16))

@@ -15,12 +15,13 @@ import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-def _strided(t: torch.Tensor, extra: int) -> torch.Tensor:
-    """t (2-D, on the CPU) copied into the first columns of a wider CUDA buffer."""
+def _strided(t: torch.Tensor, extra: int):
+    """t (2-D, on the CPU) copied into the first columns of a wider CUDA
+    buffer whose other columns hold NaN.  Returns (view, buffer)."""
     M, N = t.shape
     buf = torch.full((M, N + extra), float("nan"), dtype=t.dtype, device="cuda")
     buf[:, :N] = t.cuda()
-    return buf[:, :N]
+    return buf[:, :N], buf
 
 
 @pytest.mark.parametrize("op", ["ln", "rms"])
@@ -29,10 +30,10 @@ def test_strided_rows(op, extra):
     base = wl.WORKLOADS["ln_bf16_65536x1024" if op == "ln" else "rms_bf16_16384x4096"]
     w = base.with_shape(700, 1024)
     inp = wl.make_inputs(w)
-    x, dy = _strided(inp["x"], extra), _strided(inp["dy"], extra)
+    (x, xb), (dy, dyb) = _strided(inp["x"], extra), _strided(inp["dy"], extra)
     assert x.stride(0) == 1024 + extra
-    y = _strided(torch.zeros_like(inp["x"]), extra + 8)
-    dx = _strided(torch.zeros_like(inp["x"]), extra + 16)
+    y, yb = _strided(torch.zeros_like(inp["x"]), extra + 8)
+    dx, dxb = _strided(torch.zeros_like(inp["x"]), extra + 16)
     g = inp["gamma"].cuda()
     if op == "ln":
         b = inp["beta"].cuda()
@@ -46,6 +47,11 @@ def test_strided_rows(op, extra):
     got = {k: v.cpu().contiguous() for k, v in got.items()}
     reps = gpu_parity.compare(w, inp, got)
     assert all(r.ok() for r in reps), "\n".join(map(str, reps))
+    # nothing was written into the rows' padding, nor into the inputs
+    N = w.N
+    for name, buf in (("x", xb), ("dy", dyb), ("y", yb), ("dx", dxb)):
+        assert torch.isnan(buf[:, N:]).all(), f"{name}: the row padding was written"
+    assert torch.equal(xb[:, :N].cpu(), inp["x"]) and torch.equal(dyb[:, :N].cpu(), inp["dy"])
     assert gbn.device_error() == 0
 
 
