@@ -10,33 +10,31 @@
 // through a ring of S shared-memory stages (x row, dy row) by 1-D bulk
 // copies.  The row's reductions and its elementwise output run in different
 // warps, so no warp waits for a peer's share of a row:
-//  * warp 0, lane 0 (producer): first copies gamma (mbarrier `gbar`), then
+//  * warp 0, lane 0 (producer): copies gamma first (mbarrier `gbar`), then
 //    issues row k into stage k mod S once every output warp has released row
 //    k - S (mbarrier `consumed`, one arrival per output warp); the two
-//    copies of a row complete the stage's `full` mbarrier.  Nothing is
-//    loaded before the first copy is issued, so HBM is busy from the start.
-//  * kSumWarps sum warps: every sum warp takes every row, in row order, and
-//    sums its share of the row: 32-vector groups j, j + kSumWarps, ... (per
-//    lane one partial sum per element position, a pairwise tree over the
-//    positions, then a warp butterfly: a fixed order).  Saved statistics:
-//    sum(dyhat) (LayerNorm) and sum(dyhat * (x - mean)).  None saved:
-//    RMSNorm sum(x^2) and sum(dyhat * x); LayerNorm first sum(x) (the mean,
-//    exchanged among the sum warps through a named barrier), then
-//    sum((x - mean)^2), sum(dyhat), sum(dyhat * (x - mean)).  Lane 0 stores
-//    the partials beside the stage (sum warp 0 also the row's saved rstd and
-//    mean, loaded one row ahead, or the recomputed mean) and arrives on the
-//    stage's `ready` mbarrier (one arrival per sum warp).
+//    copies of a row complete the stage's `full` mbarrier.  It starts as
+//    soon as the barriers exist, so HBM is busy from the kernel's start.
+//  * the other warps meanwhile stage the CTA's saved statistics in shared
+//    memory (one named barrier among them).
+//  * kSumWarps sum warps: sum warp j takes whole rows j, j + kSumWarps, ...
+//    (several rows in flight, one per sum warp).  Saved statistics: it forms
+//    sum(dyhat) (LayerNorm) and sum(dyhat * (x - mean)).  None saved: the
+//    row's mean first (LayerNorm), then sum((x - mean)^2) or sum(x^2),
+//    sum(dyhat) and sum(dyhat * (x - mean)), as the forward forms them.  Per
+//    lane one partial sum per element position over the lane's vectors in
+//    order, a pairwise tree over the positions, then a warp butterfly: a
+//    fixed order.  Lane 0 stores the row's {rstd, mean, c1 = mean(dyhat),
+//    c2 = mean(dyhat * xhat)} beside the stage and arrives on its `ready`
+//    mbarrier.
 //  * kOutWarps output warps: warp o owns columns [o * VO * 32 * V, (o + 1) *
 //    VO * 32 * V) of every row.  For each row in order it waits for `ready`,
-//    adds the sum warps' partials in sum-warp order (the same bits in every
-//    output warp), forms rstd (none saved) and c1 = mean(dyhat), c2 =
-//    mean(dyhat * xhat), writes its slice of dx = dyhat*rstd + xhat*a + b with
-//    16-byte streaming stores, adds dy*xhat (and dy) into its register
-//    accumulators, and arrives on `consumed`.
+//    writes its slice of dx = dyhat*rstd + xhat*a + b with 16-byte streaming
+//    stores, adds dy*xhat (and dy) into its register accumulators, and
+//    arrives on `consumed`.
 // The output warps' columns are disjoint, so each stores its part of the
 // CTA's partial row directly.  `ready` completing implies the stage landed;
-// `consumed` completing implies every warp is done reading the stage.  All
-// roles take rows in order, so each wait's parity is unambiguous.
+// `consumed` completing implies every warp is done reading the stage.
 // Every wait is bounded (p.wait_ns, two seconds by default) and taken by all
 // lanes of a warp with one outcome: a warp that gives up records the error
 // and stops as a whole; the producer then waits (with its own bound) for its
@@ -55,22 +53,19 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
     constexpr int V = Tr::kVec;
     constexpr int E = VO * V;
     constexpr int NS = kSumWarps;
-    // partial sums a sum warp passes on per row
-    constexpr int NQ = RECOMP && LN ? 3 : 2;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int N = p.N;
-    const int groups = N / (32 * V);  // 32-vector groups of a row
+    const int nvec = N / V;
     const int S = p.stages;
     const uint32_t rowb = static_cast<uint32_t>(N) * sizeof(T);
-    const WsLayout L = ws_layout(rowb, S);
+    const WsLayout L = ws_layout(LN, rowb, S, p.stat_rows);
     unsigned char *ring = smem;
-    const unsigned char *gam_s = smem + L.gam;
-    float4 *cval = reinterpret_cast<float4 *>(smem + L.cval);  // [S][NS + 1]
-    float *xch = reinterpret_cast<float *>(smem + L.xch);      // [2][NS], by row parity
-    // [2], by row parity: a sum warp reads row k's flag after row k's
-    // exchange while a faster one may already set row k + 1's
-    volatile int *sum_abort = reinterpret_cast<volatile int *>(xch + 2 * NS);
+    unsigned char *gam_s = smem + L.gam;
+    float *st_rstd = reinterpret_cast<float *>(smem + L.stat);
+    float *st_mean = st_rstd + p.stat_rows;
+    float4 *cval = reinterpret_cast<float4 *>(smem + L.cval);  // [S]: rstd, mean, c1, c2
+    int *issued_count = reinterpret_cast<int *>(cval + S);     // rows the producer has issued
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *ready = full + S;
     uint64_t *consumed = ready + S;
@@ -84,15 +79,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&ready[i], NS);
+            mbar_init(&ready[i], 1);
             mbar_init(&consumed[i], kOutWarps);
         }
         mbar_init(gbar, 1);
-        sum_abort[0] = sum_abort[1] = 0;
+        *issued_count = 0;
         fence_barrier_init();
     }
     __syncthreads();
-    griddep_launch_dependents();
     const float inv_n = 1.0f / static_cast<float>(N);
     const uint64_t wait_ns = p.wait_ns;
 
@@ -100,10 +94,15 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
         // ---- producer
         if (lane == 0) {
             mbar_arrive_expect_tx(gbar, rowb);
-            bulk_load_nohint(const_cast<unsigned char *>(gam_s), p.gamma, rowb, gbar);
+            bulk_load_nohint(gam_s, p.gamma, rowb, gbar);
             int issued = 0;
+            bool triggered = false;
             RingPos pos;
             for (; issued < nrows; ++issued) {
+                if (issued == S) {  // the ring is in flight: let the column reduce launch
+                    griddep_launch_dependents();
+                    triggered = true;
+                }
                 if (issued >= S &&
                     !mbar_wait_bounded(&consumed[pos.stage], pos.parity ^ 1u, wait_ns)) {  // row issued - S released
                     record_error(p.err, kErrWaitFull);
@@ -117,8 +116,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
                 mbar_arrive_expect_tx(&full[pos.stage], 2 * rowb);
                 bulk_load_nohint(dst, static_cast<const T *>(p.x) + row * p.ld_x, rowb, &full[pos.stage]);
                 bulk_load_nohint(dst + rowb, static_cast<const T *>(p.dy) + row * p.ld_dy, rowb, &full[pos.stage]);
+                st_release_shared(issued_count, issued + 1);
                 pos.next(S);
             }
+            if (!triggered) griddep_launch_dependents();
             // gamma and the copies of the last S issued rows have landed
             // before the CTA may exit (earlier rows' stages were released, so
             // they landed): normally these waits return at once; after an
@@ -127,137 +128,145 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
             for (int kk = issued - S > 0 ? issued - S : 0; drained && kk < issued; ++kk)
                 drained = mbar_wait_bounded(&full[kk % S], static_cast<uint32_t>((kk / S) & 1), kDrainNs);
             if (!drained) record_error(p.err, kErrDrain);
+        } else {
+            griddep_launch_dependents();
         }
         return;
     }
 
-    if (warp <= NS) {
-        // ---- sum warp j: groups j, j + NS, ... of every row
-        const int j = warp - 1;
-        bool ok = warp_wait_bounded(gbar, 0, wait_ns);
-        // the saved statistics, loaded one row ahead (sum warp 0 passes
-        // rstd and mean on to the output warps)
-        float mu_next = 0.f, rs_next = 0.f;
-        if constexpr (!RECOMP) {
-            if (nrows > 0) {
-                if (LN) mu_next = p.mean[row0];
-                if (j == 0) rs_next = p.rstd[row0];
-            }
+    // ---- the consumer warps: this CTA's saved statistics, staged while the
+    // producer's first copies are in flight
+    if constexpr (!RECOMP) {
+        for (int i = tid - 32; i < nrows; i += static_cast<int>(blockDim.x) - 32) {
+            st_rstd[i] = p.rstd[row0 + i];
+            if (LN) st_mean[i] = p.mean[row0 + i];
         }
-        RingPos pos;
-        for (int k = 0; k < nrows; ++k) {
-            ok = ok && warp_wait_bounded(&full[pos.stage], pos.parity, wait_ns);
-            if constexpr (!(RECOMP && LN)) {
-                if (!ok) {
-                    record_error(p.err, kErrWaitFull);
-                    break;
-                }
-            }
-            const unsigned char *sx = ring + (size_t)pos.stage * 2 * rowb;
-            float mu = 0.f, rs = 0.f;
-            if constexpr (!RECOMP) {
-                mu = mu_next;
-                rs = rs_next;
-                if (k + 1 < nrows) {
-                    if (LN) mu_next = p.mean[row0 + k + 1];
-                    if (j == 0) rs_next = p.rstd[row0 + k + 1];
-                }
-            }
-            if constexpr (RECOMP && LN) {
-                // the mean first: this warp's share of sum(x), exchanged
-                // with the other sum warps (a warp whose wait ran out still
-                // joins the exchange, so none is left waiting; then all stop)
-                float ax[V];
+    }
+    named_barrier(1, static_cast<int>(blockDim.x) - 32);
+    griddep_launch_dependents();
+    bool ok = warp_wait_bounded(gbar, 0, wait_ns);  // gamma landed
+
+    if (warp <= NS) {
+        // ---- sum warp j takes rows j, j + NS, ...
+        const int j = warp - 1;
+        for (int k = j; ok && k < nrows; k += NS) {
+            const int st = k % S;
+            // Sum warps do not take rows in order, so this one may reach row k
+            // while the stage still holds row k - S, whose phase of `full`
+            // has the other parity: a wait on row k's parity would then pass
+            // at once.  Row k is issued only after row k - S was consumed,
+            // hence landed; once it is issued the parity is unambiguous.
+            ok = ok && __all_sync(0xffffffffu, wait_counter_above(issued_count, k, wait_ns)) &&
+                 warp_wait_bounded(&full[st], static_cast<uint32_t>((k / S) & 1), wait_ns);
+            if (!ok) break;
+            const unsigned char *sx = ring + (size_t)st * 2 * rowb;
+            float rs, mu = 0.f, c1, c2;
+            if constexpr (RECOMP) {
+                // no saved statistics: the mean first (LayerNorm), then the
+                // centred squares and the two sums of the backward
+                if constexpr (LN) {
+                    float ax[V];
 #pragma unroll
-                for (int e = 0; e < V; ++e) ax[e] = 0.f;
-                if (ok) {
-                    for (int g = j; g < groups; g += NS) {
+                    for (int e = 0; e < V; ++e) ax[e] = 0.f;
+#pragma unroll 2
+                    for (int v = lane; v < nvec; v += 32) {
                         float xf[V];
-                        Tr::unpack(ld_shared_v4(sx + (size_t)(g * 32 + lane) * 16), xf);
+                        Tr::unpack(ld_shared_v4(sx + (size_t)v * 16), xf);
 #pragma unroll
                         for (int e = 0; e < V; ++e) ax[e] += xf[e];
                     }
+#pragma unroll
+                    for (int w = 1; w < V; w *= 2)
+#pragma unroll
+                        for (int e = 0; e < V; e += 2 * w) ax[e] += ax[e + w];
+                    mu = warp_sum(ax[0]) * inv_n;
                 }
+                float q[V], d1[V], d2[V];  // sum((x - mean)^2), sum(dyhat), sum(dyhat * (x - mean))
 #pragma unroll
-                for (int w = 1; w < V; w *= 2)
+                for (int e = 0; e < V; ++e) q[e] = d1[e] = d2[e] = 0.f;
+#pragma unroll 2
+                for (int v = lane; v < nvec; v += 32) {
+                    float xf[V], df[V], gf[V];
+                    Tr::unpack(ld_shared_v4(sx + (size_t)v * 16), xf);
+                    Tr::unpack(ld_shared_v4(sx + rowb + (size_t)v * 16), df);
+                    Tr::unpack(ld_shared_v4(gam_s + (size_t)v * 16), gf);
 #pragma unroll
-                    for (int e = 0; e < V; e += 2 * w) ax[e] += ax[e + w];
-                const float sx_part = warp_sum(ax[0]);
-                if (lane == 0) {
-                    xch[(k & 1) * NS + j] = sx_part;
-                    if (!ok) sum_abort[k & 1] = 1;
-                }
-                named_barrier(1, 32 * NS);
-                if (sum_abort[k & 1]) {
-                    if (!ok) record_error(p.err, kErrWaitFull);
-                    break;
-                }
-                float t = xch[(k & 1) * NS];
-#pragma unroll
-                for (int q = 1; q < NS; ++q) t += xch[(k & 1) * NS + q];
-                mu = t * inv_n;
-            }
-            // one partial sum per element position (V chains of dependent
-            // adds instead of one), added in a fixed order below
-            float a0[V], a1[V], a2[NQ == 3 ? V : 1];
-#pragma unroll
-            for (int e = 0; e < V; ++e) {
-                a0[e] = a1[e] = 0.f;
-                if constexpr (NQ == 3) a2[e] = 0.f;
-            }
-            for (int g = j; g < groups; g += NS) {
-                const int v = g * 32 + lane;
-                float xf[V], df[V], gf[V];
-                Tr::unpack(ld_shared_v4(sx + (size_t)v * 16), xf);
-                Tr::unpack(ld_shared_v4(sx + rowb + (size_t)v * 16), df);
-                Tr::unpack(ld_shared_v4(gam_s + (size_t)v * 16), gf);
-#pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float dyhat = df[e] * gf[e];
-                    if constexpr (RECOMP && LN) {
+                    for (int e = 0; e < V; ++e) {
                         const float d = xf[e] - mu;
-                        a0[e] = fmaf(d, d, a0[e]);   // sum((x - mean)^2)
-                        a1[e] += dyhat;              // sum(dyhat)
-                        a2[e] = fmaf(dyhat, d, a2[e]);  // sum(dyhat * (x - mean))
-                    } else if constexpr (RECOMP) {
-                        a0[e] = fmaf(xf[e], xf[e], a0[e]);  // sum(x^2)
-                        a1[e] = fmaf(dyhat, xf[e], a1[e]);  // sum(dyhat * x)
-                    } else {
-                        if constexpr (LN) a0[e] += dyhat;                    // sum(dyhat)
-                        a1[e] = fmaf(dyhat, LN ? xf[e] - mu : xf[e], a1[e]);  // sum(dyhat * (x - mean))
+                        const float dyhat = df[e] * gf[e];
+                        q[e] = fmaf(d, d, q[e]);
+                        if constexpr (LN) d1[e] += dyhat;
+                        d2[e] = fmaf(dyhat, d, d2[e]);
                     }
                 }
-            }
 #pragma unroll
-            for (int w = 1; w < V; w *= 2) {
+                for (int w = 1; w < V; w *= 2) {
 #pragma unroll
-                for (int e = 0; e < V; e += 2 * w) {
-                    a0[e] += a0[e + w];
-                    a1[e] += a1[e + w];
-                    if constexpr (NQ == 3) a2[e] += a2[e + w];
+                    for (int e = 0; e < V; e += 2 * w) {
+                        q[e] += q[e + w];
+                        if constexpr (LN) d1[e] += d1[e + w];
+                        d2[e] += d2[e + w];
+                    }
                 }
-            }
-            float s0 = a0[0], s1 = a1[0], s2 = 0.f;
-            if constexpr (!RECOMP && !LN) {
-                s1 = warp_sum(s1);  // RMSNorm with saved rstd: no sum(dyhat)
+                float sq = q[0], s1 = d2[0], s0 = LN ? d1[0] : 0.f;
+                warp_sum2(sq, s1);
+                if constexpr (LN) s0 = warp_sum(s0);
+                rs = 1.0f / sqrtf(sq * inv_n + p.eps);
+                c1 = s0 * inv_n;
+                c2 = s1 * rs * inv_n;
             } else {
-                warp_sum2(s0, s1);
-                if constexpr (NQ == 3) s2 = warp_sum(a2[0]);
+                rs = st_rstd[k];
+                mu = LN ? st_mean[k] : 0.f;
+                // one partial sum per element position of a vector (V chains
+                // of dependent adds instead of one), added in a fixed order
+                float a0[LN ? V : 1], a1[V];  // sum(dyhat), sum(dyhat * (x - mean))
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    a1[e] = 0.f;
+                    if constexpr (LN) a0[e] = 0.f;
+                }
+#pragma unroll 2
+                for (int v = lane; v < nvec; v += 32) {
+                    float xf[V], df[V], gf[V];
+                    Tr::unpack(ld_shared_v4(sx + (size_t)v * 16), xf);
+                    Tr::unpack(ld_shared_v4(sx + rowb + (size_t)v * 16), df);
+                    Tr::unpack(ld_shared_v4(gam_s + (size_t)v * 16), gf);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float dyhat = df[e] * gf[e];
+                        if constexpr (LN) a0[e] += dyhat;
+                        a1[e] = fmaf(dyhat, LN ? xf[e] - mu : xf[e], a1[e]);
+                    }
+                }
+#pragma unroll
+                for (int w = 1; w < V; w *= 2) {
+#pragma unroll
+                    for (int e = 0; e < V; e += 2 * w) {
+                        a1[e] += a1[e + w];
+                        if constexpr (LN) a0[e] += a0[e + w];
+                    }
+                }
+                float s0 = 0.f, s1 = a1[0];
+                if constexpr (LN) {
+                    s0 = a0[0];
+                    warp_sum2(s0, s1);
+                } else {
+                    s1 = warp_sum(s1);
+                }
+                c1 = s0 * inv_n;
+                c2 = s1 * rs * inv_n;
             }
             if (lane == 0) {
-                cval[pos.stage * (NS + 1) + j] = make_float4(s0, s1, s2, 0.f);
-                if (j == 0) cval[pos.stage * (NS + 1) + NS] = make_float4(rs, mu, 0.f, 0.f);
-                mbar_arrive(&ready[pos.stage]);
+                cval[st] = make_float4(rs, mu, c1, c2);
+                mbar_arrive(&ready[st]);
             }
-            pos.next(S);
         }
+        if (!ok) record_error(p.err, kErrWaitFull);
         return;
     }
 
     // ---- output warp o: columns [o * VO * 32, (o + 1) * VO * 32) in vectors
     const int o = warp - 1 - NS;
-    bool ok = warp_wait_bounded(gbar, 0, wait_ns);
-    if (!ok) record_error(p.err, kErrWaitFull);
     float gam[E], acc_g[E], acc_b[LN ? E : 1];
 #pragma unroll
     for (int jv = 0; jv < VO; ++jv) {
@@ -274,38 +283,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
     }
     RingPos pos;
     for (int k = 0; ok && k < nrows; ++k) {
-        if (!warp_wait_bounded(&ready[pos.stage], pos.parity, wait_ns)) {
-            record_error(p.err, kErrWaitFull);
-            break;
-        }
+        ok = warp_wait_bounded(&ready[pos.stage], pos.parity, wait_ns);
+        if (!ok) break;
         const unsigned char *sx = ring + (size_t)pos.stage * 2 * rowb;
-        // the sum warps' partials, added in sum-warp order
-        const float4 *cv = cval + pos.stage * (NS + 1);
-        float4 q = cv[0];
-#pragma unroll
-        for (int jj = 1; jj < NS; ++jj) {
-            const float4 t = cv[jj];
-            q.x += t.x;
-            q.y += t.y;
-            q.z += t.z;
-        }
-        const float4 stat = cv[NS];
-        float rs, mu = stat.y, c1 = 0.f, c2;
-        if constexpr (RECOMP && LN) {
-            rs = 1.0f / sqrtf(q.x * inv_n + p.eps);
-            c1 = q.y * inv_n;
-            c2 = q.z * rs * inv_n;
-        } else if constexpr (RECOMP) {
-            rs = 1.0f / sqrtf(q.x * inv_n + p.eps);
-            c2 = q.y * rs * inv_n;
-        } else {
-            rs = stat.x;
-            if constexpr (LN) c1 = q.x * inv_n;
-            c2 = q.y * rs * inv_n;
-        }
-        // c1 = mean(dyhat), c2 = mean(dyhat * xhat)
-        const float a = -rs * c2;
-        const float b = LN ? -rs * c1 : 0.f;
+        const float4 cv = cval[pos.stage];
+        const float rs = cv.x, mu = cv.y;
+        const float a = -rs * cv.w;             // -rstd * c2
+        const float b = LN ? -rs * cv.z : 0.f;  // -rstd * c1
         T *dxrow = static_cast<T *>(p.dx) + (row0 + k) * p.ld_dx;
 #pragma unroll
         for (int jv = 0; jv < VO; ++jv) {
@@ -327,6 +311,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
         if (lane == 0) mbar_arrive(&consumed[pos.stage]);
         pos.next(S);
     }
+    if (!ok) record_error(p.err, kErrWaitFull);
     // this CTA's partial row: the warp's own columns (with p.atom_g set, the
     // atomics ablation, added into dgamma / dbeta instead)
     const bool atomic = p.atom_g != nullptr;

@@ -9,26 +9,25 @@
 
 namespace gbn {
 
-// warps of each role: one producer, kSumWarps sum warps (every row's sums
-// split over all of them), kOutWarps output warps (fixed column slices)
-constexpr int kSumWarps = 4;
+// warps of each role: one producer, kSumWarps sum warps (whole rows, taken
+// in turn), kOutWarps output warps (fixed column slices of every row)
+constexpr int kSumWarps = 5;
 constexpr int kOutWarps = 16;
 constexpr int kWsThreads = 32 * (1 + kSumWarps + kOutWarps);
 
 struct WsLayout {
-    size_t gam, cval, xch, bars, total;
+    size_t gam, stat, cval, bars, total;
 };
 
-// ring [S][2 * rowb] | gamma [rowb] | per stage: the sum warps' partial sums
-// [S][kSumWarps] float4 and the row's statistics [S] float4 |
-// save-nothing LayerNorm exchange [2][kSumWarps] floats + abort flags [2] |
+// ring [S][2 * rowb] | gamma [rowb] | saved rstd, mean [stat_rows] |
+// per stage the row's {rstd, mean, c1, c2} [S] float4, issued-row count |
 // mbarriers full, ready, consumed [S] and gamma's
-__host__ __device__ inline WsLayout ws_layout(size_t rowb, int S) {
+__host__ __device__ inline WsLayout ws_layout(bool ln, size_t rowb, int S, int stat_rows) {
     WsLayout L;
     L.gam = (size_t)S * 2 * rowb;
-    L.cval = L.gam + round_up(rowb, 16);
-    L.xch = L.cval + (size_t)S * (kSumWarps + 1) * 16;
-    L.bars = L.xch + round_up((size_t)2 * kSumWarps * 4 + 8, 16);
+    L.stat = L.gam + round_up(rowb, 16);
+    L.cval = L.stat + round_up((size_t)stat_rows * 4 * (ln ? 2 : 1), 16);
+    L.bars = L.cval + (size_t)S * 16 + 16;
     L.total = L.bars + ((size_t)3 * S + 1) * 8;
     return L;
 }

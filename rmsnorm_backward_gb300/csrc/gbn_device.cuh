@@ -180,6 +180,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// a counter in shared memory written by one thread and polled by others
+__device__ __forceinline__ void st_release_shared(int *p, int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
+// Waits until *counter > k, giving up after ~limit_ns (checked on the global
+// timer before the first poll that follows a failed look, then every 64
+// polls).  Returns false on giving up.
+__device__ __forceinline__ bool wait_counter_above(const int *counter, int k, uint64_t limit_ns) {
+    if (ld_acquire_shared(counter) > k) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if (ld_acquire_shared(counter) > k) return true;
+    }
+    return false;
+}
+
 // mbar_wait_bounded by every lane of a warp, with one outcome for the warp:
 // false if any lane gave up, so that the warp stops as a whole and no lane
 // is left behind in a later warp-wide shuffle or __syncwarp

@@ -239,25 +239,27 @@ int fwd_impl(bool ln, const void *x, const void *gamma, const void *beta, void *
 // The warp-specialised backward's launch: rows of 16 output warps x 32
 // lanes x 1-2 vectors, where it measured faster (shorter rows leave too few
 // output warps; at 4 vectors a lane the slot kernel was faster), and >= 2
-// stages.  It depends on the shape and the device only.
+// stages.  stat_rows: the saved statistics it stages per CTA (0 when none
+// were saved).
 struct WsPlan {
     bool ok = false;
-    int vo = 0, stages = 0;
+    int vo = 0, stages = 0, stat_rows = 0;
     size_t smem = 0;
 };
 
-WsPlan ws_plan(int dtype, int64_t N, const DevInfo &d) {
+WsPlan ws_plan(bool ln, int dtype, int64_t N, int stat_rows, const DevInfo &d) {
     WsPlan w;
     const int V = 16 / elem_bytes(dtype);
     int vo = 0;
     if (N % V != 0 || !ws_shape(static_cast<int>(N / V), &vo)) return w;
     const size_t rowb = (size_t)N * elem_bytes(dtype);
     for (int S = 16; S >= 2; --S) {
-        const WsLayout L = ws_layout(rowb, S);
+        const WsLayout L = ws_layout(ln, rowb, S, stat_rows);
         if (L.total <= static_cast<size_t>(d.smem_optin)) {
             w.ok = true;
             w.vo = vo;
             w.stages = S;
+            w.stat_rows = stat_rows;
             w.smem = L.total;
             break;
         }
@@ -265,13 +267,20 @@ WsPlan ws_plan(int dtype, int64_t N, const DevInfo &d) {
     return w;
 }
 
+// the statistics rows one CTA stages: ceil(M / G)
+int stat_rows_of(int64_t M, int G) { return G > 0 ? static_cast<int>((M + G - 1) / G) : 0; }
+
 // Slices of the column reduce's CTAs: 8 (256 threads) where the
 // warp-specialised kernel takes the shape, so that they fit on an SM beside
 // it and start as soon as its grid completes; 16 (512 threads) beside the
 // other kernels, which leave no room for them.  A function of the shape and
 // the device only (not of alignment or options), so every call that reduces
 // the same [G, N] partial rows sums them in the same order.
-bool colsum_small(int dtype, int64_t N, const DevInfo &d) { return ws_plan(dtype, N, d).ok; }
+bool colsum_small(int dtype, int64_t N, const DevInfo &d) {
+    const int V = 16 / elem_bytes(dtype);
+    int vo = 0;
+    return N % V == 0 && ws_shape(static_cast<int>(N / V), &vo);
+}
 
 // recompute_eps >= 0: no saved statistics (mean / rstd null), the kernels
 // form them from x with this eps; < 0: the statistics are required.
@@ -307,9 +316,10 @@ int bwd_rows_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     // the warp-specialised kernel (every reduce mode, so dx does not depend on it)
     bool launched = false;
     if (aligned && o.kernel == GBN_KERNEL_AUTO) {
-        const WsPlan w = ws_plan(dtype, N, d);
+        const WsPlan w = ws_plan(ln, dtype, N, recompute ? 0 : stat_rows_of(M, p.G), d);
         if (w.ok) {
             p.stages = w.stages;
+            p.stat_rows = w.stat_rows;
             st = cuda_status(launch_bwd_ws(dtype, ln, w.vo, p, w.smem, stream));
             launched = true;
         }
@@ -859,7 +869,7 @@ int gbn_bwd_plan(int64_t M, int64_t N, int dtype, int has_beta, int *G, int *sta
     if (G) *G = g;
     if (staged) {
         *staged = 0;
-        if (M > 0 && ws_plan(dtype, N, d).ok)
+        if (M > 0 && ws_plan(has_beta != 0, dtype, N, stat_rows_of(M, g), d).ok)
             *staged = 2;
         else if (M > 0 && staged_plan(true, has_beta != 0, dtype, M, N, g, d).ok)
             *staged = 1;

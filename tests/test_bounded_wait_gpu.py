@@ -27,10 +27,14 @@ BASE = {"ln": wl.WORKLOADS["ln_bf16_65536x1024"], "rms": wl.WORKLOADS["rms_bf16_
 
 
 @pytest.mark.parametrize("op", ["ln", "rms"])
-@pytest.mark.parametrize("kernel,N,saved", [("auto", 4096, True), ("auto", 4096, False), ("auto", 8192, True),
-                                            ("slot", 4096, True), ("slot", 1024, False)])
-def test_waits_that_run_out_report_error_1_and_the_device_stays_usable(op, kernel, N, saved):
+@pytest.mark.parametrize("N,saved", [(4096, True), (4096, False), (8192, True), (8192, False)])
+def test_waits_that_run_out_report_error_1_and_the_device_stays_usable(op, N, saved):
+    """The warp-specialised kernel: its consumer warps first wait for gamma's
+    copy, issued just before, so at a one-nanosecond limit that wait gives
+    up; the producer then gives up on the consumers and drains its copies."""
+    kernel = "auto"
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert gbn.bwd_plan(40 * sms, N, torch.bfloat16, op == "ln")[1] == 2
     # more rows per CTA than ring stages, so the producer waits on the
     # consumers too
     w = dataclasses.replace(BASE[op], dtype="bf16", M=40 * sms + 7, N=N, name=f"{op}_bf16_bounded_{N}")
