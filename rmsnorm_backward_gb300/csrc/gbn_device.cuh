@@ -386,41 +386,78 @@ struct ColsumShape {
     static constexpr int kBatch = 192 / SLICES;  // loads a thread issues together: one batch up to G = 192
 };
 
-// sum over g < G of P[g*ldp + c], for c in [c0, c1), 32 columns a
-// pass: lane q of slice s (threads 32*s + q, s < SLICES) adds rows s,
-// s + SLICES, ... in increasing order (ColsumShape::kBatch loads issued
-// together), then slice 0 adds the slice sums in slice order.  Every CTA
-// shape with the same SLICES gives the same bits per column.  Needs at
-// least 32 * SLICES threads (the others only join the barriers) and
-// sm[SLICES][33].  P is read through L2 (written by an earlier grid).
-// store(c, sum) writes the result of column c.
-template <int SLICES, typename Store>
+// VEC consecutive fp32 values from L2, VEC = 1, 2 or 4 (address aligned to
+// 4 * VEC bytes)
+template <int VEC>
+__device__ __forceinline__ void ldcg_vec(const float *p, float (&v)[VEC]) {
+    if constexpr (VEC == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(p));
+        v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+    } else if constexpr (VEC == 2) {
+        const float2 t = __ldcg(reinterpret_cast<const float2 *>(p));
+        v[0] = t.x, v[1] = t.y;
+    } else {
+        v[0] = __ldcg(p);
+    }
+}
+
+// sum over g < G of P[g*ldp + c], for c in [c0, c1), 32 * VEC columns a
+// pass: lane q of slice s (threads 32*s + q, s < SLICES) holds columns
+// cb + VEC*q .. cb + VEC*q + VEC-1 and adds rows s, s + SLICES, ... of each
+// in increasing order (ColsumShape::kBatch loads of VEC values issued
+// together), then slice 0 adds the slice sums in slice order.  Each
+// column's order depends on SLICES only, so every VEC and CTA shape with
+// the same SLICES gives the same bits per column.  Needs at least
+// 32 * SLICES threads (the others only join the barriers),
+// sm[SLICES * (32 * VEC + 1)], P aligned to 4 * VEC bytes and ldp a
+// multiple of VEC (a lane's VEC values then never cross the end of a
+// partial row: columns from N up to ldp are padding that is read, never
+// stored).  P is read through L2 (written by an earlier grid).  store(c,
+// sum) writes the result of column c.
+template <int SLICES, int VEC, typename Store>
 __device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int c0, int c1, Store store,
-                                             float (*sm)[33]) {
+                                             float *sm) {
     constexpr int kColsumSlices = SLICES;
     constexpr int kColsumBatch = ColsumShape<SLICES>::kBatch;
+    constexpr int W = 32 * VEC + 1;  // row pitch of sm
     const int q = threadIdx.x & 31, slice = threadIdx.x >> 5;
-    for (int cb = c0; cb < c1; cb += 32) {
-        const int c = cb + q;
-        float a = 0.f;
+    for (int cb = c0; cb < c1; cb += 32 * VEC) {
+        const int c = cb + q * VEC;
+        float a[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) a[j] = 0.f;
         if (slice < kColsumSlices && c < c1) {
             for (int g0 = slice; g0 < G; g0 += kColsumSlices * kColsumBatch) {
-                float v[kColsumBatch];
+                float v[kColsumBatch][VEC];
 #pragma unroll
                 for (int u = 0; u < kColsumBatch; ++u) {
                     const int g = g0 + u * kColsumSlices;
-                    v[u] = g < G ? __ldcg(P + (size_t)g * ldp + c) : 0.f;
+                    if (g < G) {
+                        ldcg_vec<VEC>(P + (size_t)g * ldp + c, v[u]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) v[u][j] = 0.f;
+                    }
                 }
 #pragma unroll
-                for (int u = 0; u < kColsumBatch; ++u) a += v[u];
+                for (int u = 0; u < kColsumBatch; ++u)
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) a[j] += v[u][j];
             }
         }
-        if (slice < kColsumSlices) sm[slice][q] = a;
+        if (slice < kColsumSlices)
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) sm[slice * W + q * VEC + j] = a[j];
         __syncthreads();
-        if (slice == 0 && c < c1) {
-            float t = sm[0][q];
-            for (int s2 = 1; s2 < kColsumSlices; ++s2) t += sm[s2][q];
-            store(c, t);
+        if (slice == 0) {
+#pragma unroll
+            for (int i = q; i < 32 * VEC; i += 32) {
+                if (cb + i < c1) {
+                    float t = sm[i];
+                    for (int s2 = 1; s2 < kColsumSlices; ++s2) t += sm[s2 * W + i];
+                    store(cb + i, t);
+                }
+            }
         }
         __syncthreads();
     }

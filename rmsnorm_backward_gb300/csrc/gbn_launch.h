@@ -128,9 +128,10 @@ cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_
 cudaError_t launch_bwd_ws(int dtype, bool ln, int vo, const BwdParams &p, size_t smem, cudaStream_t s);
 // dgamma / dbeta from the partial rows; out_dtype is GBN_F32 or the storage
 // dtype of the parameters (rounded to nearest even); accumulate adds the
-// buffers' previous contents (widened) to the sums before the store
+// buffers' previous contents (widened) to the sums before the store; sms:
+// the device's SM count (the grid shape, not the order, depends on it)
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
-                          bool accumulate, bool small, cudaStream_t s);
+                          bool accumulate, bool small, int sms, cudaStream_t s);
 
 // reduction ablation: dgamma (dbeta) = sum over rows of dy*xhat (dy), each CTA
 // owning 32 columns and walking every row of x and dy in order

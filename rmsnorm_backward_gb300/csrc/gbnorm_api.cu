@@ -360,7 +360,7 @@ int reduce_impl(const void *workspace, size_t workspace_bytes_given, int64_t M, 
     const int G = grid_rows(M, d);
     return cuda_status(launch_colsum(workspace_partials(const_cast<void *>(workspace)), G, partial_ld(N),
                                      static_cast<int>(N), dgamma, ln ? dbeta : nullptr, o.grad_dtype,
-                                     o.accumulate, colsum_small(dtype, N, d), stream));
+                                     o.accumulate, colsum_small(dtype, N, d), d.sms, stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -537,7 +537,7 @@ int bwd_host_impl(bool ln, const void *dy, const void *x, const void *gamma, con
     }
     if (ok) {
         ok = chk(launch_colsum(part, static_cast<int>(h.Gtot), ldp, static_cast<int>(N), grad,
-                               ln ? grad + N : nullptr, GBN_F32, false, colsum_small(dtype, N, d), s)) &&
+                               ln ? grad + N : nullptr, GBN_F32, false, colsum_small(dtype, N, d), d.sms, s)) &&
              chk(cudaMemcpyAsync(dgamma, grad, (size_t)N * 4, cudaMemcpyDeviceToHost, s)) &&
              (!ln || chk(cudaMemcpyAsync(dbeta, grad + N, (size_t)N * 4, cudaMemcpyDeviceToHost, s))) &&
              chk(cudaEventRecord(dx_out, hs.out)) && chk(cudaStreamWaitEvent(s, dx_out, 0));

@@ -17,21 +17,21 @@ namespace gbn {
 static __device__ int g_error_flag = 0;
 
 // dgamma (blockIdx.y = 0) or dbeta (blockIdx.y = 1): CTA x sums columns
-// [32x, 32x + 32) of the partial rows with colsum_range (one fixed order per
-// SLICES).
-template <typename OutT, bool ACC, int SLICES>
+// [32*VEC*x, 32*VEC*(x + 1)) of the partial rows with colsum_range (one
+// fixed order per SLICES, whatever VEC).
+template <typename OutT, bool ACC, int SLICES, int VEC>
 __global__ void __launch_bounds__(32 * SLICES) colsum_kernel(const float *__restrict__ part, int G, int ldp,
                                                                      int N, OutT *__restrict__ dgamma,
                                                                      OutT *__restrict__ dbeta) {
-    __shared__ float sm[SLICES][33];
+    __shared__ float sm[SLICES * (32 * VEC + 1)];
     griddep_wait();  // the partial rows of the kernel before this one
     const float *P = part + (size_t)blockIdx.y * G * ldp;
     OutT *out = blockIdx.y ? dbeta : dgamma;
-    const int c0 = blockIdx.x * 32;
+    const int c0 = blockIdx.x * 32 * VEC;
     // accumulate: the buffer's previous value is added after the fixed-order
     // sum; 16-bit outputs are rounded to nearest even
-    colsum_range<SLICES>(
-        P, G, ldp, c0, min(N, c0 + 32),
+    colsum_range<SLICES, VEC>(
+        P, G, ldp, c0, min(N, c0 + 32 * VEC),
         [&](int c, float t) {
             if constexpr (std::is_same<OutT, float>::value) {
                 out[c] = ACC ? out[c] + t : t;
@@ -123,10 +123,10 @@ cudaError_t launch_bwd_plain(int dtype, bool ln, const BwdParams &p, cudaStream_
     return cudaErrorInvalidValue;
 }
 
-template <typename OutT, bool ACC, int SLICES>
+template <typename OutT, bool ACC, int SLICES, int VEC>
 cudaError_t launch_colsum_t(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + 31) / 32, dbeta ? 2 : 1);
+    cfg.gridDim = dim3((N + 32 * VEC - 1) / (32 * VEC), dbeta ? 2 : 1);
     cfg.blockDim = dim3(32 * SLICES);
     cfg.stream = s;
     // launched as a programmatic dependent of the rows kernel before it
@@ -135,26 +135,44 @@ cudaError_t launch_colsum_t(const float *part, int G, int ldp, int N, void *dgam
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, colsum_kernel<OutT, ACC, SLICES>, part, G, ldp, N, static_cast<OutT *>(dgamma),
-                              static_cast<OutT *>(dbeta));
+    return cudaLaunchKernelEx(&cfg, colsum_kernel<OutT, ACC, SLICES, VEC>, part, G, ldp, N,
+                              static_cast<OutT *>(dgamma), static_cast<OutT *>(dbeta));
+}
+
+template <typename OutT, bool ACC, int SLICES>
+cudaError_t launch_colsum_v(const float *part, int G, int ldp, int N, void *dg, void *db, int vec, cudaStream_t s) {
+    if constexpr (SLICES == 8) {
+        if (vec == 4) return launch_colsum_t<OutT, ACC, SLICES, 4>(part, G, ldp, N, dg, db, s);
+        if (vec == 2) return launch_colsum_t<OutT, ACC, SLICES, 2>(part, G, ldp, N, dg, db, s);
+    }
+    return launch_colsum_t<OutT, ACC, SLICES, 1>(part, G, ldp, N, dg, db, s);
 }
 
 template <typename OutT>
 cudaError_t launch_colsum_acc(const float *part, int G, int ldp, int N, void *dg, void *db, bool acc, bool small,
-                              cudaStream_t s) {
+                              int vec, cudaStream_t s) {
     if (small)
-        return acc ? launch_colsum_t<OutT, true, 8>(part, G, ldp, N, dg, db, s)
-                   : launch_colsum_t<OutT, false, 8>(part, G, ldp, N, dg, db, s);
-    return acc ? launch_colsum_t<OutT, true, 16>(part, G, ldp, N, dg, db, s)
-               : launch_colsum_t<OutT, false, 16>(part, G, ldp, N, dg, db, s);
+        return acc ? launch_colsum_v<OutT, true, 8>(part, G, ldp, N, dg, db, vec, s)
+                   : launch_colsum_v<OutT, false, 8>(part, G, ldp, N, dg, db, vec, s);
+    return acc ? launch_colsum_v<OutT, true, 16>(part, G, ldp, N, dg, db, vec, s)
+               : launch_colsum_v<OutT, false, 16>(part, G, ldp, N, dg, db, vec, s);
 }
 
+// vec: columns a lane sums (1, 2 or 4).  8 slices: the fewest that keep the
+// grid to one CTA per SM, so a wide partial block is read in one wave of
+// loads (1151x8192 f16 LayerNorm: 1.2 us less than one column a lane).  16
+// slices stay at one column a lane: with four the compiler kept fewer loads
+// in flight (8192x16384 RMSNorm: 1.1 us more).
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
-                          bool accumulate, bool small, cudaStream_t s) {
+                          bool accumulate, bool small, int sms, cudaStream_t s) {
+    const int arrays = dbeta ? 2 : 1;
+    int vec = 1;
+    while (small && vec < 4 && (int64_t)((N + 32 * vec - 1) / (32 * vec)) * arrays > sms) vec *= 2;
+    if (ldp % vec != 0 || (reinterpret_cast<uintptr_t>(part) & (4 * vec - 1)) != 0) vec = 1;
     switch (out_dtype) {
-        case 0: return launch_colsum_acc<float>(part, G, ldp, N, dgamma, dbeta, accumulate, small, s);
-        case 1: return launch_colsum_acc<__half>(part, G, ldp, N, dgamma, dbeta, accumulate, small, s);
-        case 2: return launch_colsum_acc<__nv_bfloat16>(part, G, ldp, N, dgamma, dbeta, accumulate, small, s);
+        case 0: return launch_colsum_acc<float>(part, G, ldp, N, dgamma, dbeta, accumulate, small, vec, s);
+        case 1: return launch_colsum_acc<__half>(part, G, ldp, N, dgamma, dbeta, accumulate, small, vec, s);
+        case 2: return launch_colsum_acc<__nv_bfloat16>(part, G, ldp, N, dgamma, dbeta, accumulate, small, vec, s);
     }
     return cudaErrorInvalidValue;
 }

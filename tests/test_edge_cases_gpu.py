@@ -1,4 +1,6 @@
 """Edge cases of the CUDA path against the oracle (needs a GPU)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -15,7 +17,6 @@ BASE = {"ln": wl.WORKLOADS["ln_f32_64x256"], "rms": wl.WORKLOADS["rms_bf16_16384
 
 def _w(op, dtype, M, N, eps=None):
     b = BASE[op]
-    import dataclasses
     return dataclasses.replace(b, dtype=dtype, M=M, N=N, eps=eps if eps is not None else b.eps,
                                name=f"{op}_{dtype}_{M}x{N}")
 
@@ -153,13 +154,15 @@ def _view(t: torch.Tensor, misalign: bool) -> torch.Tensor:
 
 
 @pytest.mark.parametrize("op", ["ln", "rms"])
-@pytest.mark.parametrize("N", [2048, 4096])
+@pytest.mark.parametrize("N", [2048, 4096, 8192])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_two_phases_equal_the_fused_call(op, N, misalign):
-    """The phase calls (rows, then reduce) give the fused call's bits.  With
-    x and dy one element off a 16-byte boundary the rows go through the
-    plain kernel; the column reduce's order depends on the shape only, so
-    the phase call, which does not know the rows kernel, still matches."""
+    """The phase calls (rows, then reduce) give the fused call's bits.  N =
+    4096 and 8192 take the warp-specialised rows kernel, 2048 the slot
+    kernel.  With x and dy one element off a 16-byte boundary the rows go
+    through the plain kernel; the column reduce's order depends on the
+    shape only, so the phase call, which does not know the rows kernel,
+    still matches."""
     w = _w(op, "bf16", 1000, N)
     inp = wl.make_inputs(w)
     d = {k: v.cuda() for k, v in inp.items()}
@@ -244,4 +247,33 @@ def test_reused_workspace_keeps_working():
         dx, dg = gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(dg, dg0) and torch.equal(dx, dx0)
+    assert gbn.device_error() == 0
+
+
+@pytest.mark.parametrize("op", ["ln", "rms"])
+def test_workspace_shared_by_alternating_problems(op):
+    """Two different problems take turns on one workspace: every call gives
+    the bits of the same problem run on a fresh workspace, never a mix with
+    the other problem's partial rows."""
+    base = wl.WORKLOADS["ln_bf16_65536x1024" if op == "ln" else "rms_bf16_16384x4096"]
+    probs = []
+    for seed in (3, 4):
+        w = dataclasses.replace(base.with_shape(3000, 4096), seed=seed)
+        d = {k: v.cuda() for k, v in wl.make_inputs(w).items()}
+        if op == "ln":
+            _, mean, rstd = gbn.ln_fwd(d["x"], d["gamma"], d["beta"], w.eps)
+            run = (lambda d, mean, rstd: lambda ws: gbn.ln_bwd(d["dy"], d["x"], d["gamma"], mean, rstd,
+                                                                workspace=ws))(d, mean, rstd)
+        else:
+            _, rstd = gbn.rms_fwd(d["x"], d["gamma"], w.eps)
+            run = (lambda d, rstd: lambda ws: gbn.rms_bwd(d["dy"], d["x"], d["gamma"], rstd, workspace=ws))(d, rstd)
+        probs.append(run)
+    nbytes = gbn.bwd_workspace_bytes(3000, 4096, torch.bfloat16, op == "ln")
+    fresh = [[t.clone() for t in run(torch.empty(nbytes, dtype=torch.uint8, device="cuda"))] for run in probs]
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    for i in range(12):
+        got = probs[i % 2](ws)
+        for a, b in zip(fresh[i % 2], got):
+            assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a.view(torch.int32),
+                               b.view(torch.int16) if b.dtype != torch.float32 else b.view(torch.int32)), i
     assert gbn.device_error() == 0

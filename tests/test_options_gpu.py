@@ -57,9 +57,10 @@ def test_strided_rows(op, extra):
 
 @pytest.mark.parametrize("op", ["ln", "rms"])
 @pytest.mark.parametrize("grad_dtype", ["f32", "bf16"])
-def test_accumulate_and_grad_dtype(op, grad_dtype):
+@pytest.mark.parametrize("N", [2048, 4096])  # the slot and the warp-specialised rows kernel
+def test_accumulate_and_grad_dtype(op, grad_dtype, N):
     base = wl.WORKLOADS["ln_bf16_65536x1024" if op == "ln" else "rms_bf16_16384x4096"]
-    w = base.with_shape(900, 2048)
+    w = base.with_shape(900, N)
     inp = wl.make_inputs(w)
     d = {k: v.cuda() for k, v in inp.items()}
     gdt = wl.TORCH_DTYPES[grad_dtype]
