@@ -35,6 +35,11 @@
 // The output warps' columns are disjoint, so each stores its part of the
 // CTA's partial row directly.  `ready` completing implies the stage landed;
 // `consumed` completing implies every warp is done reading the stage.
+// Both the sum and the output warps do their float32 arithmetic in packed
+// pairs of elements (fma / mul / add .f32x2): the same operations in the
+// same order as the scalar form, so the same bits, in half the issues -- the
+// sum warps share the SM's issue slots with the output warps and set the
+// row rate, so fewer issues per row is a shorter kernel.
 // Every wait is bounded (p.wait_ns, two seconds by default) and taken by all
 // lanes of a warp with one outcome: a warp that gives up records the error
 // and stops as a whole; the producer then waits (with its own bound) for its
@@ -165,25 +170,31 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
                 // no saved statistics: the mean first (LayerNorm), then the
                 // centred squares and the two sums of the backward
                 if constexpr (LN) {
-                    float ax[V];
+                    float2 axp[V / 2];
 #pragma unroll
-                    for (int e = 0; e < V; ++e) ax[e] = 0.f;
+                    for (int i = 0; i < V / 2; ++i) axp[i] = make_float2(0.f, 0.f);
 #pragma unroll 2
                     for (int v = lane; v < nvec; v += 32) {
                         float xf[V];
                         Tr::unpack(ld_shared_v4(sx + (size_t)v * 16), xf);
 #pragma unroll
-                        for (int e = 0; e < V; ++e) ax[e] += xf[e];
+                        for (int i = 0; i < V / 2; ++i) axp[i] = pair_add(axp[i], pair_at(xf, i));
                     }
+                    float ax[V];
+#pragma unroll
+                    for (int i = 0; i < V / 2; ++i) ax[2 * i] = axp[i].x, ax[2 * i + 1] = axp[i].y;
 #pragma unroll
                     for (int w = 1; w < V; w *= 2)
 #pragma unroll
                         for (int e = 0; e < V; e += 2 * w) ax[e] += ax[e + w];
                     mu = warp_sum(ax[0]) * inv_n;
                 }
-                float q[V], d1[V], d2[V];  // sum((x - mean)^2), sum(dyhat), sum(dyhat * (x - mean))
+                // sum((x - mean)^2), sum(dyhat), sum(dyhat * (x - mean)), in
+                // pairs of element positions
+                float2 qp[V / 2], d1p[V / 2], d2p[V / 2];
 #pragma unroll
-                for (int e = 0; e < V; ++e) q[e] = d1[e] = d2[e] = 0.f;
+                for (int i = 0; i < V / 2; ++i) qp[i] = d1p[i] = d2p[i] = make_float2(0.f, 0.f);
+                const float2 nmu = make_float2(-mu, -mu);
 #pragma unroll 2
                 for (int v = lane; v < nvec; v += 32) {
                     float xf[V], df[V], gf[V];
@@ -191,13 +202,20 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
                     Tr::unpack(ld_shared_v4(sx + rowb + (size_t)v * 16), df);
                     Tr::unpack(ld_shared_v4(gam_s + (size_t)v * 16), gf);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        const float d = xf[e] - mu;
-                        const float dyhat = df[e] * gf[e];
-                        q[e] = fmaf(d, d, q[e]);
-                        if constexpr (LN) d1[e] += dyhat;
-                        d2[e] = fmaf(dyhat, d, d2[e]);
+                    for (int i = 0; i < V / 2; ++i) {
+                        const float2 d = LN ? pair_add(pair_at(xf, i), nmu) : pair_at(xf, i);
+                        const float2 dyhat = pair_mul(pair_at(df, i), pair_at(gf, i));
+                        qp[i] = pair_fma(d, d, qp[i]);
+                        if constexpr (LN) d1p[i] = pair_add(d1p[i], dyhat);
+                        d2p[i] = pair_fma(dyhat, d, d2p[i]);
                     }
+                }
+                float q[V], d1[V], d2[V];
+#pragma unroll
+                for (int i = 0; i < V / 2; ++i) {
+                    q[2 * i] = qp[i].x, q[2 * i + 1] = qp[i].y;
+                    d1[2 * i] = d1p[i].x, d1[2 * i + 1] = d1p[i].y;
+                    d2[2 * i] = d2p[i].x, d2[2 * i + 1] = d2p[i].y;
                 }
 #pragma unroll
                 for (int w = 1; w < V; w *= 2) {
@@ -218,13 +236,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
                 rs = st_rstd[k];
                 mu = LN ? st_mean[k] : 0.f;
                 // one partial sum per element position of a vector (V chains
-                // of dependent adds instead of one), added in a fixed order
-                float a0[LN ? V : 1], a1[V];  // sum(dyhat), sum(dyhat * (x - mean))
+                // of dependent adds instead of one), added in a fixed order,
+                // in pairs of positions
+                float2 a0p[V / 2], a1p[V / 2];  // sum(dyhat), sum(dyhat * (x - mean))
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    a1[e] = 0.f;
-                    if constexpr (LN) a0[e] = 0.f;
-                }
+                for (int i = 0; i < V / 2; ++i) a0p[i] = a1p[i] = make_float2(0.f, 0.f);
+                const float2 nmu = make_float2(-mu, -mu);
 #pragma unroll 2
                 for (int v = lane; v < nvec; v += 32) {
                     float xf[V], df[V], gf[V];
@@ -232,11 +249,17 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
                     Tr::unpack(ld_shared_v4(sx + rowb + (size_t)v * 16), df);
                     Tr::unpack(ld_shared_v4(gam_s + (size_t)v * 16), gf);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        const float dyhat = df[e] * gf[e];
-                        if constexpr (LN) a0[e] += dyhat;
-                        a1[e] = fmaf(dyhat, LN ? xf[e] - mu : xf[e], a1[e]);
+                    for (int i = 0; i < V / 2; ++i) {
+                        const float2 dyhat = pair_mul(pair_at(df, i), pair_at(gf, i));
+                        if constexpr (LN) a0p[i] = pair_add(a0p[i], dyhat);
+                        a1p[i] = pair_fma(dyhat, LN ? pair_add(pair_at(xf, i), nmu) : pair_at(xf, i), a1p[i]);
                     }
+                }
+                float a0[LN ? V : 1], a1[V];
+#pragma unroll
+                for (int i = 0; i < V / 2; ++i) {
+                    a1[2 * i] = a1p[i].x, a1[2 * i + 1] = a1p[i].y;
+                    if constexpr (LN) a0[2 * i] = a0p[i].x, a0[2 * i + 1] = a0p[i].y;
                 }
 #pragma unroll
                 for (int w = 1; w < V; w *= 2) {
@@ -290,6 +313,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
         const float rs = cv.x, mu = cv.y;
         const float a = -rs * cv.w;             // -rstd * c2
         const float b = LN ? -rs * cv.z : 0.f;  // -rstd * c1
+        const float2 rs2 = make_float2(rs, rs), a2 = make_float2(a, a), b2 = make_float2(b, b);
+        const float2 nmu2 = make_float2(-mu, -mu);
         T *dxrow = static_cast<T *>(p.dx) + (row0 + k) * p.ld_dx;
 #pragma unroll
         for (int jv = 0; jv < VO; ++jv) {
@@ -297,12 +322,22 @@ __global__ void __launch_bounds__(kWsThreads, 1) bwd_ws_kernel(const BwdParams p
             float xf[V], df[V], out[V];
             Tr::unpack(ld_shared_v4(sx + (size_t)v * 16), xf);
             Tr::unpack(ld_shared_v4(sx + rowb + (size_t)v * 16), df);
+            // in pairs of elements: xhat, the dgamma (dbeta) accumulators and
+            // dx = (dy*gamma)*rstd + (xhat*a + b)
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                const float xhat = LN ? (xf[e] - mu) * rs : xf[e] * rs;
-                acc_g[jv * V + e] = fmaf(df[e], xhat, acc_g[jv * V + e]);
-                if constexpr (LN) acc_b[jv * V + e] += df[e];
-                out[e] = fmaf(df[e] * gam[jv * V + e], rs, LN ? fmaf(xhat, a, b) : xhat * a);
+            for (int i = 0; i < V / 2; ++i) {
+                const int e = jv * V + 2 * i;
+                const float2 d2 = pair_at(df, i);
+                const float2 xh = LN ? pair_mul(pair_add(pair_at(xf, i), nmu2), rs2) : pair_mul(pair_at(xf, i), rs2);
+                const float2 ag = pair_fma(d2, xh, make_float2(acc_g[e], acc_g[e + 1]));
+                acc_g[e] = ag.x, acc_g[e + 1] = ag.y;
+                if constexpr (LN) {
+                    const float2 ab = pair_add(make_float2(acc_b[e], acc_b[e + 1]), d2);
+                    acc_b[e] = ab.x, acc_b[e + 1] = ab.y;
+                }
+                const float2 dg = pair_mul(d2, make_float2(gam[e], gam[e + 1]));
+                const float2 o2 = pair_fma(dg, rs2, LN ? pair_fma(xh, a2, b2) : pair_mul(xh, a2));
+                out[2 * i] = o2.x, out[2 * i + 1] = o2.y;
             }
             st_global_cs_v4(dxrow + (size_t)v * V, Tr::pack(out));
         }

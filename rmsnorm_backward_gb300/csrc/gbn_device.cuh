@@ -386,6 +386,39 @@ struct ColsumShape {
     static constexpr int kBatch = 192 / SLICES;  // loads a thread issues together: one batch up to G = 192
 };
 
+// Packed float32 pairs (sm_100 and later: fma / mul / add on .f32x2): each
+// half rounds as the scalar instruction would, so a pair computes exactly
+// what two scalar operations compute, in one issue.
+__device__ __forceinline__ float2 pair_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 pair_mul(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 pair_add(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// elements 2i, 2i+1 of an unpacked vector as a pair
+__device__ __forceinline__ float2 pair_at(const float *f, int i) { return make_float2(f[2 * i], f[2 * i + 1]); }
+
 // VEC consecutive fp32 values from L2, VEC = 1, 2 or 4 (address aligned to
 // 4 * VEC bytes)
 template <int VEC>
