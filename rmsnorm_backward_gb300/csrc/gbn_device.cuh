@@ -465,7 +465,18 @@ __device__ __forceinline__ void colsum_range(const float *P, int G, int ldp, int
 #pragma unroll
                 for (int u = 0; u < kColsumBatch; ++u) {
                     const int g = g0 + u * kColsumSlices;
-                    if (g < G) {
+                    if constexpr (VEC == 1) {
+                        // every load is issued (rows past the end read the
+                        // last row again and count as 0), so the compiler
+                        // keeps the whole batch in flight: 65536x1024
+                        // LayerNorm 1.4 us faster than a branch per load
+                        float t[1];
+                        ldcg_vec<1>(P + (size_t)(g < G ? g : G - 1) * ldp + c, t);
+                        v[u][0] = g < G ? t[0] : 0.f;
+                    } else if (g < G) {
+                        // wider lanes keep the branch: with the unconditional
+                        // form the compiler interleaved loads and adds and
+                        // 1151x8192 LayerNorm lost 4.4 us
                         ldcg_vec<VEC>(P + (size_t)g * ldp + c, v[u]);
                     } else {
 #pragma unroll

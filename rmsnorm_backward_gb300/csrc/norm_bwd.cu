@@ -143,7 +143,6 @@ template <typename OutT, bool ACC, int SLICES>
 cudaError_t launch_colsum_v(const float *part, int G, int ldp, int N, void *dg, void *db, int vec, cudaStream_t s) {
     if constexpr (SLICES == 8) {
         if (vec == 4) return launch_colsum_t<OutT, ACC, SLICES, 4>(part, G, ldp, N, dg, db, s);
-        if (vec == 2) return launch_colsum_t<OutT, ACC, SLICES, 2>(part, G, ldp, N, dg, db, s);
     }
     return launch_colsum_t<OutT, ACC, SLICES, 1>(part, G, ldp, N, dg, db, s);
 }
@@ -158,16 +157,16 @@ cudaError_t launch_colsum_acc(const float *part, int G, int ldp, int N, void *dg
                : launch_colsum_v<OutT, false, 16>(part, G, ldp, N, dg, db, vec, s);
 }
 
-// vec: columns a lane sums (1, 2 or 4).  8 slices: the fewest that keep the
-// grid to one CTA per SM, so a wide partial block is read in one wave of
-// loads (1151x8192 f16 LayerNorm: 1.2 us less than one column a lane).  16
-// slices stay at one column a lane: with four the compiler kept fewer loads
-// in flight (8192x16384 RMSNorm: 1.1 us more).
+// vec: columns a lane sums (1 or 4).  8 slices: four when one would need
+// more CTAs than SMs, so a wide partial block is read in one wave of loads
+// (1151x8192 f16 LayerNorm: 1.2 us less than one column a lane).  16 slices
+// stay at one column a lane: with four the compiler kept fewer loads in
+// flight (8192x16384 RMSNorm: 1.1 us more).
 cudaError_t launch_colsum(const float *part, int G, int ldp, int N, void *dgamma, void *dbeta, int out_dtype,
                           bool accumulate, bool small, int sms, cudaStream_t s) {
     const int arrays = dbeta ? 2 : 1;
     int vec = 1;
-    while (small && vec < 4 && (int64_t)((N + 32 * vec - 1) / (32 * vec)) * arrays > sms) vec *= 2;
+    if (small && (int64_t)((N + 31) / 32) * arrays > sms) vec = 4;
     if (ldp % vec != 0 || (reinterpret_cast<uintptr_t>(part) & (4 * vec - 1)) != 0) vec = 1;
     switch (out_dtype) {
         case 0: return launch_colsum_acc<float>(part, G, ldp, N, dgamma, dbeta, accumulate, small, vec, s);
