@@ -21,13 +21,35 @@ CASES = [  # (workload family, dtype, M, N): staged kernels, then plain-load one
     ("ln_f32_64x256", "f32", 64, 256),
     ("ln_bf16_65536x1024", "bf16", 300, 1000),
     ("rms_bf16_16384x4096", "f32", 100, 333),
+    # rows with large means next to their spread, in float32: the
+    # statistics formed inside the kernels must not lose the variance to
+    # cancellation
+    ("ln_bf16_65536x1024", "f32", 300, 1024),
+    ("ln_bf16_65536x1024", "f32", 200, 2000),
+    ("ln_bf16_65536x1024", "bf16", 153, 16384),
 ]
 
 
 @pytest.mark.parametrize("family,dtype,M,N", CASES)
 def test_backward_without_saved_statistics(family, dtype, M, N):
+    _check_recompute(family, dtype, M, N)
+
+
+@pytest.mark.parametrize("dtype,N", [("f32", 1024), ("bf16", 1024), ("f32", 4096)])
+def test_backward_without_saved_statistics_outlier_first_column(dtype, N):
+    """Column 0 of every row far from the rest (an outlier channel at the
+    first feature): the statistics formed inside the kernels (the mean
+    first, then the centred sums) keep their accuracy."""
+    def bend(inp):
+        inp["x"][:, 0] = inp["x"][:, 0] * 64 + 300
+    _check_recompute("ln_bf16_65536x1024", dtype, 300, N, bend)
+
+
+def _check_recompute(family, dtype, M, N, bend=None):
     w = dataclasses.replace(wl.WORKLOADS[family], dtype=dtype, M=M, N=N, name=f"{family}-{dtype}-{M}x{N}")
     inp = wl.make_inputs(w)
+    if bend is not None:
+        bend(inp)
     d = {k: v.cuda() for k, v in inp.items()}
     x, dy, g = (wl.exact_double(inp[k]) for k in ("x", "dy", "gamma"))
     if w.op == "ln":
