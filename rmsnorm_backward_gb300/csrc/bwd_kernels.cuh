@@ -301,6 +301,68 @@ __global__ void __launch_bounds__(kRingThreads, 1) bwd_staged_kernel(const BwdPa
             pos.next(S);
             continue;
         }
+        if constexpr (RECOMP && !LN && MODE == kHoldX) {
+            // RMSNorm with no saved statistics, x held as raw vectors: pass 1
+            // forms sum(x^2) and sum(dyhat*x) together (one exchange gives
+            // rstd and c2 = rstd*sum(dyhat*x)/N) and holds dy itself; pass 2
+            // adds dy*xhat into the dgamma accumulators and writes dx =
+            // dy*gamma*rstd + x*(rstd*a), gamma from shared memory
+            const unsigned char *sx = ring + (size_t)pos.stage * stage_bytes + (size_t)ts * 16;
+            const unsigned char *sdy = sx + rowb;
+            uint4 xr[NV];
+            float dyv[E];
+            float r[2] = {0.f, 0.f};  // sum(x^2), sum(dyhat*x)
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                float xf[V], gl[V];
+                if (FULL || ts + j * tpr < nvec) {
+                    xr[j] = *reinterpret_cast<const uint4 *>(sx + j * vstride);
+                    Tr::unpack(xr[j], xf);
+                    Tr::unpack(*reinterpret_cast<const uint4 *>(sdy + j * vstride), dyv + j * V);
+                    const float *gs = gam_s + (size_t)(ts + j * tpr) * V;
+#pragma unroll
+                    for (int e = 0; e < V; e += 4) {
+                        const float4 t = *reinterpret_cast<const float4 *>(gs + e);
+                        gl[e] = t.x, gl[e + 1] = t.y, gl[e + 2] = t.z, gl[e + 3] = t.w;
+                    }
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        r[0] = fmaf(xf[e], xf[e], r[0]);
+                        r[1] = fmaf(dyv[j * V + e] * gl[e], xf[e], r[1]);
+                    }
+                } else {
+                    xr[j] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) dyv[j * V + e] = 0.f;
+                }
+            }
+            if (slot_reduce<2>(r, red + (k & 1) * 2 * kRedStride, flag, timed_out, W, warp, lane, 1 + slot, tpr))
+                break;
+            if (ts == 0 && issued < ns) {  // the row is in registers: refill its stage
+                fence_proxy_async();
+                issue();
+            }
+            const float rs = 1.0f / sqrtf(r[0] * inv_n + p.eps);
+            const float ax = (-rs * (rs * (r[1] * inv_n))) * rs;  // xhat*a = x*(rstd*a)
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (FULL || ts + j * tpr < nvec) {
+                    float xf[V], o[V];
+                    Tr::unpack(xr[j], xf);
+                    const float *gs = gam_s + (size_t)(ts + j * tpr) * V;
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float dyv_e = dyv[j * V + e];
+                        acc_g[j * V + e] = fmaf(dyv_e, xf[e] * rs, acc_g[j * V + e]);
+                        o[e] = fmaf(dyv_e * gs[e], rs, xf[e] * ax);
+                    }
+                    st_global_cs_v4(dxrow + (size_t)j * tpr * V, Tr::pack(o));
+                }
+            }
+            dxrow += row_step;
+            pos.next(S);
+            continue;
+        }
         const int i = slot + k * slots;
         const unsigned char *sx = ring + (size_t)pos.stage * stage_bytes + (size_t)ts * 16;
         const unsigned char *sdy = sx + rowb;
