@@ -27,6 +27,8 @@ CASES = [  # (workload family, dtype, M, N): staged kernels, then plain-load one
     ("ln_bf16_65536x1024", "f32", 300, 1024),
     ("ln_bf16_65536x1024", "f32", 200, 2000),
     ("ln_bf16_65536x1024", "bf16", 153, 16384),
+    # RMSNorm with x held as raw vectors, the last vectors of a row unowned
+    ("rms_bf16_8192x16384", "bf16", 100, 16000),
 ]
 
 
