@@ -228,8 +228,13 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// barrier over `count` threads (a multiple of 32) of this CTA, id in 1..15
+// barrier over `count` threads (a multiple of 32) of this CTA, id in 1..15.
+// bar.sync is the aligned form: each participating warp must execute it
+// converged.  Callers often reach it right after a branch taken by one lane
+// (lane 0 storing a warp's sum), and a warp need not reconverge after a
+// branch on its own, so the warp is reconverged first.
 __device__ __forceinline__ void named_barrier(int id, int count) {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
