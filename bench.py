@@ -480,6 +480,11 @@ def run_ours(args):
     fwd_bytes = wl.fwd_min_bytes(w.op, w.dtype, w.M, w.N)
     value = world * K * bwd_bytes / bwd_s / 1e9
     peak, peak_src = measured_hbm_peak()
+    # an ncu record applies to the configuration it was captured in: saved or
+    # recomputed statistics with the partial-row reduce (the ablations have none)
+    traffic_key = None
+    if args.reduce == "partials":
+        traffic_key = w.name if args.stats != "recompute" else "recompute_" + w.name
     # the fused per-row kernel: all algorithmic bytes but the dgamma/dbeta writes
     rows_bytes = bwd_bytes - 4 * w.N * (2 if w.has_beta else 1)
     rows_avg = rows_s / K
@@ -525,7 +530,7 @@ def run_ours(args):
             "bwd_min_bytes": bwd_bytes,
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name, kernel),
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(traffic_key, kernel),
                 "kernel": (f"{kernel} (dx + per-CTA partial rows) alone, against the measured copy rate"
                            if prob.rows_alone() else
                            "the whole backward call (ablation, forced kernel or save-nothing variant)"),
