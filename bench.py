@@ -60,6 +60,9 @@ def parse_args(argv=None):
                     help="the rows kernel of the public backward: the fastest that applies, or a forced one")
     ap.add_argument("--activation", choices=["silu", "gelu"], default=None,
                     help="time the activation backward on a 16384 x 4096 bf16 tensor instead of the norm")
+    ap.add_argument("--steady", action="store_true",
+                    help="time --steps public backward calls back to back, no L2 flush (workloads whose x and dy "
+                         "exceed the L2): steady state, each call paying the previous call's dx write-back")
     return ap.parse_args(argv)
 
 
@@ -764,8 +767,81 @@ def run_act_reference(args):
     }), flush=True)
 
 
+def run_steady(args):
+    """Back-to-back public backward calls with no L2 flush between them.
+
+    Valid where x and dy together are larger than L2: a call reads its rows
+    in the order the previous call read them, so it finds none of the
+    previous call's inputs there.
+    What it adds to the flushed per-call timing of the default run: the dx
+    lines a call leaves dirty in L2 are written back while the next call
+    streams its own reads, inside the timed region."""
+    rank, world, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.workload]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    in_bytes = 2 * w.M * w.N * wl.ELEM_BYTES[w.dtype]
+    if in_bytes <= l2:
+        raise SystemExit(f"{w.name}: x and dy ({in_bytes} bytes) fit in the L2 ({l2} bytes)")
+    stream = torch.cuda.Stream(device)
+    prob = Problem(w, device, stream, recompute=args.stats == "recompute", reduce=args.reduce, kernel=args.kernel)
+    flush = L2Flush(device)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    K = args.steps
+    with torch.cuda.stream(stream):
+        flush()
+        prob.fwd()
+        for _ in range(max(args.warmup, 3)):
+            prob.bwd_fused()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index, enabled=not args.no_clocks) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K):
+                prob.bwd_fused()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    err = prob.gbn.device_error(clear=True, device=device)
+    if err:
+        raise SystemExit(f"kernel error flag set: {err}")
+    t = dist_max(e0.elapsed_time(e1) / 1e3, world, device)
+    bwd_bytes = wl.bwd_min_bytes(w.op, w.dtype, w.M, w.N)
+    if args.stats == "recompute":
+        bwd_bytes -= 4 * w.M * (2 if w.has_beta else 1)
+    value = world * K * bwd_bytes / t / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(t / K * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "stats": args.stats, "reduce": args.reduce,
+                       "kernel": args.kernel,
+                       "timing": ("steady state: K public backward calls back to back between two events, no L2 "
+                                  "flush; x and dy exceed the L2")},
+            "bwd_us": round(t / K * 1e6, 3),
+            "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "pct_of_measured_copy": round(100 * value / world / measured_hbm_peak()[0], 2),
+            "gpu_launches": 2 * K,
+            "clocks": clk.summary(),
+        }), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.steady:
+        run_steady(args)
+        return
     if args.activation and args.impl == "reference":
         run_act_reference(args)
     elif args.activation:
